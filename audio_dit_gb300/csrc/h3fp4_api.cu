@@ -1,0 +1,250 @@
+// C ABI of the h3fp4 library: argument validation, workspace layout, device
+// check and kernel dispatch.  No entry point allocates device memory or
+// synchronises a stream (h3fp4_check excepted, which exists to do so).
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "h3fp4_internal.h"
+
+namespace h3fp4 {
+
+namespace {
+std::atomic<uint64_t> g_wait_limit_ns{2000000000ull};
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_dev_once[kMaxDevices];
+int g_dev_ok[kMaxDevices];
+int g_dev_sms[kMaxDevices];
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+h3fp4_status check_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return H3FP4_ERR_CUDA;
+    std::call_once(g_dev_once[dev], [dev] {
+        int major = 0, minor = 0, sms = 0;
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        g_dev_ok[dev] = (major == 10 && minor == 3) ? 1 : 0;
+        g_dev_sms[dev] = sms;
+    });
+    return g_dev_ok[dev] ? H3FP4_OK : H3FP4_ERR_UNSUPPORTED_DEVICE;
+}
+
+// Copies and validates the host segment table.
+h3fp4_status make_segments(const int64_t* seg_off, int nseg, int64_t rows, Segments* out)
+{
+    std::memset(out, 0, sizeof(*out));
+    if (seg_off == nullptr) {
+        if (nseg > 1) return H3FP4_ERR_INVALID;
+        out->nseg = 1;
+        out->off[0] = 0;
+        out->off[1] = rows;
+        return H3FP4_OK;
+    }
+    if (nseg < 1 || nseg > H3FP4_MAX_SEGMENTS) return H3FP4_ERR_SHAPE;
+    if (seg_off[0] != 0 || seg_off[nseg] != rows) return H3FP4_ERR_INVALID;
+    for (int i = 0; i < nseg; ++i)
+        if (seg_off[i + 1] < seg_off[i]) return H3FP4_ERR_INVALID;
+    out->nseg = nseg;
+    for (int i = 0; i <= nseg; ++i) out->off[i] = seg_off[i];
+    return H3FP4_OK;
+}
+
+h3fp4_status check_shape(int64_t rows, int64_t K)
+{
+    if (rows < 1 || K < 64 || K % 64 != 0 || K > (int64_t)kMaxPartials * 1024) return H3FP4_ERR_SHAPE;
+    if (rows > (int64_t)INT32_MAX || K > (int64_t)INT32_MAX / 2) return H3FP4_ERR_SHAPE;
+    if (rows * (K / 8) > (int64_t)INT32_MAX * 8) return H3FP4_ERR_SHAPE;
+    return H3FP4_OK;
+}
+
+h3fp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? H3FP4_OK : H3FP4_ERR_CUDA; }
+
+}  // namespace
+
+int sm_count_current_device()
+{
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < kMaxDevices && g_dev_sms[dev] > 0) return g_dev_sms[dev];
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms > 0 ? sms : 1;
+}
+
+}  // namespace h3fp4
+
+using namespace h3fp4;
+
+extern "C" {
+
+size_t h3fp4_codes_bytes(int64_t rows, int64_t K)
+{
+    if (rows < 0 || K < 0) return 0;
+    return (size_t)rows * (size_t)K / 2;
+}
+
+size_t h3fp4_sf_bytes(int64_t rows, int64_t K)
+{
+    if (rows < 0 || K < 0) return 0;
+    return (size_t)((rows + 127) / 128) * 128 * (size_t)((K / 16 + 3) / 4) * 4;
+}
+
+size_t h3fp4_workspace_bytes(int64_t M, int64_t N, int64_t K, int flags)
+{
+    (void)N;
+    size_t bytes = kWsActCodes;
+    if (!(flags & H3FP4_A_PREQUANT)) bytes += round256(h3fp4_codes_bytes(M, K)) + round256(h3fp4_sf_bytes(M, K));
+    return bytes;
+}
+
+void h3fp4_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
+
+const char* h3fp4_status_string(h3fp4_status s)
+{
+    switch (s) {
+    case H3FP4_OK: return "ok";
+    case H3FP4_ERR_INVALID: return "invalid argument";
+    case H3FP4_ERR_SHAPE: return "unsupported shape (K % 64, N % 8, rows >= 1, segments)";
+    case H3FP4_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case H3FP4_ERR_CUDA: return "CUDA error";
+    case H3FP4_ERR_TIMEOUT: return "device wait timed out";
+    case H3FP4_ERR_UNSUPPORTED_DEVICE: return "device is not sm_103 (GB300)";
+    }
+    return "unknown status";
+}
+
+h3fp4_status h3fp4_quantize_act(const void* x_bf16, int64_t M, int64_t K, const float* shift, const float* scale,
+                                const int64_t* seg_off, int nseg, void* codes, void* sf, float* gscale, int flags,
+                                void* ws, cudaStream_t stream)
+{
+    h3fp4_status st = check_shape(M, K);
+    if (st != H3FP4_OK) return st;
+    if (!x_bf16 || !codes || !sf || !gscale || !ws) return H3FP4_ERR_INVALID;
+    if (flags & ~(H3FP4_PROLOGUE_MOD | H3FP4_GSCALE_GIVEN)) return H3FP4_ERR_INVALID;
+    const bool mod = (flags & H3FP4_PROLOGUE_MOD) != 0;
+    if (mod && (!shift || !scale)) return H3FP4_ERR_INVALID;
+    if (!aligned16(x_bf16) || !aligned16(codes) || !aligned16(sf) || !aligned16(ws) ||
+        (reinterpret_cast<uintptr_t>(gscale) & 3u) || (mod && (!aligned16(shift) || !aligned16(scale))))
+        return H3FP4_ERR_ALIGN;
+    QuantJob job{};
+    st = make_segments(seg_off, nseg <= 0 ? 1 : nseg, M, &job.seg);
+    if (st != H3FP4_OK) return st;
+    if ((st = check_device()) != H3FP4_OK) return st;
+    job.x = x_bf16;
+    job.rows = M;
+    job.K = K;
+    job.shift = mod ? shift : nullptr;
+    job.scale = mod ? scale : nullptr;
+    job.codes = static_cast<uint8_t*>(codes);
+    job.sf = static_cast<uint8_t*>(sf);
+    job.gscale = gscale;
+    job.gscale_given = (flags & H3FP4_GSCALE_GIVEN) != 0;
+    job.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWsPartials);
+    return from_cuda(launch_quantize(job, stream));
+}
+
+h3fp4_status h3fp4_quantize_weight(const void* w_bf16, int64_t N, int64_t K, void* codes, void* sf,
+                                   float* w_gscale, void* ws, cudaStream_t stream)
+{
+    if (N % 8 != 0) return H3FP4_ERR_SHAPE;
+    return h3fp4_quantize_act(w_bf16, N, K, nullptr, nullptr, nullptr, 1, codes, sf, w_gscale, 0, ws, stream);
+}
+
+h3fp4_status h3fp4_linear(const void* x, const void* a_sf, const float* a_gscale, int64_t M, int64_t N, int64_t K,
+                          const void* w_codes, const void* w_sf, const float* w_gscale, const float* shift,
+                          const float* scale, const float* gate, const int64_t* seg_off, int nseg,
+                          const void* bias_bf16, const void* resid_bf16, void* out_bf16, int flags, void* ws,
+                          cudaStream_t stream)
+{
+    h3fp4_status st = check_shape(M, K);
+    if (st != H3FP4_OK) return st;
+    if (N < 8 || N % 8 != 0 || N > (int64_t)INT32_MAX) return H3FP4_ERR_SHAPE;
+    const int known = H3FP4_PROLOGUE_MOD | H3FP4_EPI_BIAS | H3FP4_EPI_GATE_RESID | H3FP4_GSCALE_GIVEN |
+                      H3FP4_A_PREQUANT;
+    if (flags & ~known) return H3FP4_ERR_INVALID;
+    const bool prequant = (flags & H3FP4_A_PREQUANT) != 0;
+    const bool mod = (flags & H3FP4_PROLOGUE_MOD) != 0;
+    const bool bias = (flags & H3FP4_EPI_BIAS) != 0;
+    const bool gated = (flags & H3FP4_EPI_GATE_RESID) != 0;
+    const bool given = (flags & H3FP4_GSCALE_GIVEN) != 0;
+    if (!x || !w_codes || !w_sf || !w_gscale || !out_bf16 || !ws) return H3FP4_ERR_INVALID;
+    if (prequant && (mod || !a_sf || !a_gscale)) return H3FP4_ERR_INVALID;
+    if (given && !a_gscale) return H3FP4_ERR_INVALID;
+    if (mod && (!shift || !scale)) return H3FP4_ERR_INVALID;
+    if (bias && !bias_bf16) return H3FP4_ERR_INVALID;
+    if (gated && (!gate || !resid_bf16)) return H3FP4_ERR_INVALID;
+    if (out_bf16 == x || (gated && out_bf16 == resid_bf16)) return H3FP4_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(w_codes) || !aligned16(w_sf) || !aligned16(out_bf16) || !aligned16(ws) ||
+        (prequant && !aligned16(a_sf)) || (bias && !aligned16(bias_bf16)) ||
+        (gated && (!aligned16(gate) || !aligned16(resid_bf16))) || (mod && (!aligned16(shift) || !aligned16(scale))))
+        return H3FP4_ERR_ALIGN;
+    Segments seg;
+    st = make_segments(seg_off, nseg <= 0 ? 1 : nseg, M, &seg);
+    if (st != H3FP4_OK) return st;
+    if ((st = check_device()) != H3FP4_OK) return st;
+
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    GemmJob g{};
+    if (prequant) {
+        g.a_codes = static_cast<const uint8_t*>(x);
+        g.a_sf = static_cast<const uint8_t*>(a_sf);
+        g.a_gscale = a_gscale;
+    } else {
+        QuantJob q{};
+        q.x = x;
+        q.rows = M;
+        q.K = K;
+        q.shift = mod ? shift : nullptr;
+        q.scale = mod ? scale : nullptr;
+        q.seg = seg;
+        q.codes = wsb + kWsActCodes;
+        q.sf = q.codes + round256(h3fp4_codes_bytes(M, K));
+        q.gscale = given ? const_cast<float*>(a_gscale) : reinterpret_cast<float*>(wsb + kWsActGscale);
+        q.gscale_given = given;
+        q.partials = reinterpret_cast<float*>(wsb + kWsPartials);
+        if ((st = from_cuda(launch_quantize(q, stream))) != H3FP4_OK) return st;
+        g.a_codes = q.codes;
+        g.a_sf = q.sf;
+        g.a_gscale = q.gscale;
+    }
+    g.w_codes = static_cast<const uint8_t*>(w_codes);
+    g.w_sf = static_cast<const uint8_t*>(w_sf);
+    g.w_gscale = w_gscale;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.bias = bias ? bias_bf16 : nullptr;
+    g.gate = gated ? gate : nullptr;
+    g.resid = gated ? resid_bf16 : nullptr;
+    g.out = out_bf16;
+    g.seg = seg;
+    g.status = reinterpret_cast<unsigned int*>(wsb + kWsStatus);
+    g.wait_limit_ns = g_wait_limit_ns.load();
+    return from_cuda(launch_gemm(g, stream));
+}
+
+h3fp4_status h3fp4_check(void* ws, cudaStream_t stream)
+{
+    if (!ws) return H3FP4_ERR_INVALID;
+    unsigned int word = 0;
+    unsigned int* dev = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + kWsStatus);
+    if (cudaMemcpyAsync(&word, dev, sizeof(word), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return H3FP4_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return H3FP4_ERR_CUDA;
+    if (word != 0) {
+        if (cudaMemsetAsync(dev, 0, sizeof(word), stream) != cudaSuccess) return H3FP4_ERR_CUDA;
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return H3FP4_ERR_CUDA;
+        return H3FP4_ERR_TIMEOUT;
+    }
+    return H3FP4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// Internal declarations shared by the h3fp4 translation units (not part of the ABI).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/h3fp4.h"
+
+namespace h3fp4 {
+
+// Workspace layout (bytes from the workspace base, each region 256-aligned).
+constexpr size_t kWsStatus = 0;         // uint32 device status word (+ padding)
+constexpr size_t kWsPartials = 256;     // fp32 amax partial maxima
+constexpr int kMaxPartials = 4096;
+constexpr size_t kWsActGscale = kWsPartials + 4 * kMaxPartials;  // fp32 activation global scale
+constexpr size_t kWsActCodes = kWsActGscale + 256;                // activation codes, then block scales
+
+// Device status bits (workspace status word).
+constexpr unsigned int kStatusTimeoutProducer = 1u;
+constexpr unsigned int kStatusTimeoutMma = 2u;
+constexpr unsigned int kStatusTimeoutEpilogue = 4u;
+constexpr unsigned int kStatusBadSmemAlign = 8u;
+
+struct Segments {
+    int nseg;
+    long long off[H3FP4_MAX_SEGMENTS + 1];
+};
+
+struct QuantJob {
+    const void* x;          // bf16 [rows][K]
+    int64_t rows, K;
+    const float* shift;     // [nseg][K] or null (no prologue)
+    const float* scale;
+    Segments seg;
+    uint8_t* codes;         // [rows][K/2]
+    uint8_t* sf;            // sf_bytes(rows, K)
+    float* gscale;          // device fp32 (in if given, else out)
+    bool gscale_given;
+    float* partials;        // kMaxPartials floats
+};
+
+// Launches the amax pass (unless gscale_given) and the pack pass.
+cudaError_t launch_quantize(const QuantJob& job, cudaStream_t s);
+
+struct GemmJob {
+    const uint8_t* a_codes;  // [M][K/2]
+    const uint8_t* a_sf;
+    const float* a_gscale;
+    const uint8_t* w_codes;  // [N][K/2]
+    const uint8_t* w_sf;
+    const float* w_gscale;
+    int64_t M, N, K;
+    const void* bias;        // bf16 [N] or null
+    const float* gate;       // fp32 [nseg][N] or null
+    const void* resid;       // bf16 [M][N] or null
+    void* out;               // bf16 [M][N]
+    Segments seg;
+    unsigned int* status;    // device status word
+    uint64_t wait_limit_ns;
+};
+
+cudaError_t launch_gemm(const GemmJob& job, cudaStream_t s);
+
+int sm_count_current_device();
+
+}  // namespace h3fp4

@@ -1,0 +1,165 @@
+/*
+ * h3fp4 -- NVFP4 linear path for GB300 (sm_103a), C ABI.
+ *
+ * One linear layer of a joint video/audio diffusion transformer (QKV,
+ * attention output, MLP FC1, MLP FC2) computed as
+ *
+ *     m   = bf16(x * (1 + scale[seg]) + shift[seg])        (optional AdaLN prologue)
+ *     A   = NVFP4(m)    W = NVFP4(w)                      (16-element E4M3 blocks,
+ *                                                          fp32 global scales)
+ *     y   = (s_a * s_w) * (A_q . W_q^T)                   (fp32 accumulation)
+ *     out = bf16(R + g[seg] * (y + b))  or  bf16(y + b)   (bias + residual gate)
+ *
+ * Sources (page title / section):
+ *   "H3 Runtime Current State", "Owned Performance Kernels": the scale/pack/GEMM
+ *     paths, the block-scale swizzle at every projection width, tensor
+ *     scale/QDATA/SFA, alpha applied before the BF16 cast, the allocation-free
+ *     caller-owned "_into" producer, one full-activation scale, modulation fused
+ *     into scale/pack with exact BF16 values, and the removal of intermediate
+ *     traffic across the scale/pack/GEMM boundaries;
+ *   "H3 Runtime Current State", "Implemented And Validated": fused modulation
+ *     and residual gates;
+ *   "H3 Blackwell Runtime Plan", "Next Performance Plan: Blackwell NVFP4
+ *     GEMMs": qdata + cuBLAS tiled block-scale layout, signed zero,
+ *     tie-to-even FP4 rounding; residual, norms and modulation stay BF16.
+ *
+ * Data formats
+ *   bf16 tensors      row-major, contiguous, 16-byte aligned base.
+ *   codes             [rows][K/2] bytes; byte j of a row holds element 2j in
+ *                     bits 0-3 and element 2j+1 in bits 4-7 (E2M1: sign bit 3,
+ *                     magnitudes {0,0.5,1,1.5,2,3,4,6}).
+ *   sf (block scales) E4M3 bytes, one per (row, 16-element block), stored in
+ *                     128x4 tiles of 512 bytes:
+ *                       offset(r, c) = ((r/128)*(K/64) + c/4)*512
+ *                                      + (r%32)*16 + ((r%128)/32)*4 + c%4
+ *                     rows padded to a multiple of 128 with zero bytes.
+ *   global scale      one fp32 in DEVICE memory: s = amax / (6*448), or 1 for
+ *                     an all-zero tensor.  Dequantised value = e2m1 * e4m3 * s.
+ *
+ * Quantiser (bit-exact contract, every step one IEEE fp32 round-to-nearest op):
+ *   bmax = max|m| over the block; S = e4m3_rne_sat((bmax / 6) / s);
+ *   eff = S * s; r = (eff == 0) ? 0 : min(1 / eff, FLT_MAX);
+ *   q_i = e2m1_rne_sat(m_i * r), sign kept (negative values that round to
+ *   zero give -0).  Inputs must be finite.
+ *
+ * Common rules
+ *   - Every device buffer is caller-owned; the library never allocates
+ *     device memory and never synchronises the stream.
+ *   - All calls are asynchronous on `stream`; the return value reports host
+ *     validation and launch errors only.  Device-side wait timeouts are
+ *     recorded in the workspace status word; read them with h3fp4_check().
+ *   - Shapes: K % 64 == 0, N % 8 == 0, rows >= 1; 16-byte aligned pointers
+ *     (codes, sf, bf16 tensors, workspace); violations return
+ *     H3FP4_ERR_SHAPE / H3FP4_ERR_ALIGN and launch nothing.
+ *   - Only sm_103 devices are accepted (H3FP4_ERR_UNSUPPORTED_DEVICE
+ *     otherwise).  There is no CPU fallback and no other backend.
+ */
+#ifndef H3FP4_H
+#define H3FP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define H3FP4_API __attribute__((visibility("default")))
+#else
+#define H3FP4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    H3FP4_OK = 0,
+    H3FP4_ERR_INVALID = 1,            /* null pointer, bad flag combination, bad segments */
+    H3FP4_ERR_SHAPE = 2,              /* K % 64, N % 8, rows < 1, too many segments       */
+    H3FP4_ERR_ALIGN = 3,              /* a pointer is not 16-byte aligned                 */
+    H3FP4_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed                */
+    H3FP4_ERR_TIMEOUT = 5,            /* a bounded device wait ran out (h3fp4_check)      */
+    H3FP4_ERR_UNSUPPORTED_DEVICE = 6  /* the current device is not sm_103                 */
+} h3fp4_status;
+
+enum {
+    H3FP4_PROLOGUE_MOD = 1,    /* apply m = bf16(fma(x, 1 + scale[seg][k], shift[seg][k]))        */
+    H3FP4_EPI_BIAS = 2,        /* add bias[n] (bf16)                                               */
+    H3FP4_EPI_GATE_RESID = 4,  /* out = R[m][n] + gate[seg][n] * v   (gate fp32 [nseg][N])         */
+    H3FP4_GSCALE_GIVEN = 16,   /* activation global scale read from a_gscale (device fp32 > 0)     */
+    H3FP4_A_PREQUANT = 32      /* x is already NVFP4: codes + a_sf + a_gscale                     */
+};
+
+#define H3FP4_MAX_SEGMENTS 8
+
+/* Bytes of the E2M1 codes of a [rows, K] operand: rows * K / 2. */
+H3FP4_API size_t h3fp4_codes_bytes(int64_t rows, int64_t K);
+
+/* Bytes of the block-scale tiles of a [rows, K] operand:
+ * ceil(rows/128) * 128 * (K/64) * 4. */
+H3FP4_API size_t h3fp4_sf_bytes(int64_t rows, int64_t K);
+
+/* Workspace bytes h3fp4_linear needs for (M, N, K, flags); also enough for
+ * h3fp4_quantize_act / h3fp4_quantize_weight of M (or N) rows.  Holds the
+ * device status word, the amax partial maxima and, unless A_PREQUANT, the
+ * activation's codes, block scales and global scale.  Zero the first 256
+ * bytes (the status word) once before first use; concurrent calls must not
+ * share one workspace. */
+H3FP4_API size_t h3fp4_workspace_bytes(int64_t M, int64_t N, int64_t K, int flags);
+
+/* Quantise a weight W [N, K] bf16 to NVFP4 (offline step; same algorithm as
+ * the activations, no prologue).  Writes codes [N][K/2], sf
+ * (h3fp4_sf_bytes(N, K)) and *w_gscale (device).  ws: h3fp4_workspace_bytes
+ * (N, 0, K, 0) bytes. */
+H3FP4_API h3fp4_status h3fp4_quantize_weight(const void* w_bf16, int64_t N, int64_t K,
+                                   void* codes, void* sf, float* w_gscale,
+                                   void* ws, cudaStream_t stream);
+
+/* Quantise an activation X [M, K] bf16.
+ *   shift, scale: fp32 [nseg][K] (device), required with H3FP4_PROLOGUE_MOD.
+ *   seg_off: HOST array of nseg + 1 row offsets, seg_off[0] = 0,
+ *            non-decreasing, seg_off[nseg] = M; NULL means one segment.
+ *            1 <= nseg <= H3FP4_MAX_SEGMENTS.
+ *   flags: H3FP4_PROLOGUE_MOD, H3FP4_GSCALE_GIVEN (then *gscale is an input;
+ *          otherwise it is written with amax/(6*448) over all segments).
+ *   codes [M][K/2], sf (h3fp4_sf_bytes(M, K)), gscale: device outputs. */
+H3FP4_API h3fp4_status h3fp4_quantize_act(const void* x_bf16, int64_t M, int64_t K,
+                                const float* shift, const float* scale,
+                                const int64_t* seg_off, int nseg,
+                                void* codes, void* sf, float* gscale,
+                                int flags, void* ws, cudaStream_t stream);
+
+/* The NVFP4 linear: out[M][N] (bf16) from X and a quantised weight.
+ *   x: bf16 [M][K], or codes [M][K/2] with H3FP4_A_PREQUANT (then a_sf and
+ *      a_gscale describe it).  With H3FP4_GSCALE_GIVEN a_gscale (device) is
+ *      the activation global scale; otherwise it may be NULL and the scale is
+ *      computed (one amax over all rows and segments).
+ *   w_codes/w_sf/w_gscale: output of h3fp4_quantize_weight.
+ *   shift/scale: as in h3fp4_quantize_act (with H3FP4_PROLOGUE_MOD).
+ *   gate: fp32 [nseg][N] and resid: bf16 [M][N], with H3FP4_EPI_GATE_RESID.
+ *   bias: bf16 [N], with H3FP4_EPI_BIAS.
+ *   out may not alias x, resid or the weights. */
+H3FP4_API h3fp4_status h3fp4_linear(const void* x, const void* a_sf, const float* a_gscale,
+                          int64_t M, int64_t N, int64_t K,
+                          const void* w_codes, const void* w_sf, const float* w_gscale,
+                          const float* shift, const float* scale, const float* gate,
+                          const int64_t* seg_off, int nseg,
+                          const void* bias_bf16, const void* resid_bf16, void* out_bf16,
+                          int flags, void* ws, cudaStream_t stream);
+
+/* Synchronises `stream`, reads and clears the workspace status word.
+ * Returns H3FP4_OK, or H3FP4_ERR_TIMEOUT when a kernel gave up early (a
+ * bounded device wait ran out, or shared memory came up misaligned); the
+ * outputs of that call are then undefined. */
+H3FP4_API h3fp4_status h3fp4_check(void* ws, cudaStream_t stream);
+
+/* Maximum wait of every device-side spin in nanoseconds (default 2e9).
+ * Process-wide; meant for tests of the timeout path. */
+H3FP4_API void h3fp4_set_wait_limit_ns(uint64_t ns);
+
+/* Human-readable status. */
+H3FP4_API const char* h3fp4_status_string(h3fp4_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* H3FP4_H */

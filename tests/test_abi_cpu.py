@@ -1,0 +1,78 @@
+"""The C-ABI library builds, loads and exports every symbol include/h3fp4.h
+declares; host-side size queries and argument validation (no GPU needed)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "h3fp4.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"H3FP4_API\s+[\w\s\*]*?\b(h3fp4_\w+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from audio_dit_gb300 import build
+    build.build()
+    import audio_dit_gb300 as A
+    return A.load_library()
+
+
+def test_header_declares_the_path(lib):
+    names = declared_functions()
+    for must in ["h3fp4_quantize_weight", "h3fp4_quantize_act", "h3fp4_linear"]:
+        assert must in names
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/h3fp4.h but not exported"
+
+
+def test_size_queries(lib):
+    import audio_dit_gb300 as A
+    assert A.h3fp4_codes_bytes(256, 512) == 256 * 256
+    assert A.h3fp4_sf_bytes(1, 64) == 128 * 4
+    assert A.h3fp4_sf_bytes(129, 3072) == 256 * 3072 // 16
+    ws = A.h3fp4_workspace_bytes(300, 1024, 512, 0)
+    assert ws >= A.h3fp4_codes_bytes(300, 512) + A.h3fp4_sf_bytes(300, 512)
+    assert A.h3fp4_workspace_bytes(300, 1024, 512, A.A_PREQUANT) < ws
+
+
+def test_host_validation_rejects_before_launch(lib):
+    # shape/flag/pointer errors are decided on the host and launch nothing
+    vp = C.c_void_p
+    dummy = vp(4096)
+    assert lib.h3fp4_quantize_act(dummy, 16, 100, None, None, None, 1, dummy, dummy, dummy, 0, dummy, None) == 2
+    assert lib.h3fp4_quantize_act(dummy, 0, 64, None, None, None, 1, dummy, dummy, dummy, 0, dummy, None) == 2
+    assert lib.h3fp4_quantize_act(None, 16, 64, None, None, None, 1, dummy, dummy, dummy, 0, dummy, None) == 1
+    assert lib.h3fp4_quantize_act(vp(4097), 16, 64, None, None, None, 1, dummy, dummy, dummy, 0, dummy, None) == 3
+    # prologue without vectors
+    assert lib.h3fp4_quantize_act(dummy, 16, 64, None, None, None, 1, dummy, dummy, dummy, 1, dummy, None) == 1
+    # bad segment table (must start at 0 and end at M)
+    seg = (C.c_int64 * 3)(0, 5, 17)
+    assert lib.h3fp4_quantize_act(dummy, 16, 64, None, None, C.cast(seg, vp), 2, dummy, dummy, dummy, 0,
+                                  dummy, None) == 1
+    # N % 8
+    assert lib.h3fp4_linear(dummy, None, None, 16, 12, 64, dummy, dummy, dummy, None, None, None, None, 1,
+                            None, None, dummy, 0, dummy, None) == 2
+    # gate without residual
+    assert lib.h3fp4_linear(dummy, None, None, 16, 16, 64, dummy, dummy, dummy, None, None, dummy, None, 1,
+                            None, None, dummy, 4, dummy, None) == 1
+    # unknown flag bits
+    assert lib.h3fp4_linear(dummy, None, None, 16, 16, 64, dummy, dummy, dummy, None, None, None, None, 1,
+                            None, None, dummy, 1 << 10, dummy, None) == 1
+    assert lib.h3fp4_status_string(5) == b"device wait timed out"
+
+
+def test_product_does_not_touch_oracle():
+    """The product package never imports the oracle (or any CPU fallback)."""
+    pkg = os.path.join(ROOT, "audio_dit_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "orc_" not in text, f
