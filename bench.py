@@ -1,0 +1,424 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4 linear path on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+AdaLN modulation (when the workload has it) -> global amax -> E4M3 block
+scales + E2M1 codes -> block-scaled FP4 GEMM -> bias / residual-gate epilogue,
+inputs resident in HBM.  Metric: fused NVFP4 linear TFLOPS (2*M*N*K per step).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config qkv|tiny|fc1|fc2|attn_out]
+  python bench.py --impl reference ...   # the CPU oracle on a bounded sample
+
+Multi-GPU (torchrun, one rank per GPU): independent replicas, each rank runs
+the same per-GPU workload (weak scaling, no data-path collective); the timing
+is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused NVFP4 linear TFLOPS (% GB300 FP4 peak); act-quant GB/s (% HBM), 1 GPU"
+L2_FLUSH_BYTES = 256 << 20
+FP4_OVER_BF16 = 6.0   # nominal dense fp4 / bf16 tensor ratio (13.5 / 2.25 PFLOP/s)
+DEFAULT_CONFIG = "qkv"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={','.join(self.FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- GPU arm
+
+class Problem:
+    """Device-resident inputs and outputs of one workload."""
+
+    def __init__(self, name: str, torch, A):
+        import workloads as W
+        self.name = name
+        d = W.make_inputs(name)
+        self.d = d
+        self.M, self.N, self.K = d["M"], d["N"], d["K"]
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+        f32 = lambda a: None if a is None else torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
+        self.x = dev(d["x"])
+        self.shift, self.scale, self.gate = f32(d["shift"]), f32(d["scale"]), f32(d["gate"])
+        self.resid = None if d["resid"] is None else dev(d["resid"])
+        self.bias = dev(d["bias"])
+        self.seg_off = [int(v) for v in d["seg_off"]]
+        w = dev(d["w"])
+        self.wq = A.alloc_nvfp4(self.N, self.K)
+        self.ws = A.alloc_workspace(max(self.M, self.N), self.N, self.K, 0)
+        A.h3fp4_quantize_weight(w, *self.wq, self.ws)
+        del w
+        self.aq = A.alloc_nvfp4(self.M, self.K)
+        self.out = torch.empty((self.M, self.N), dtype=torch.bfloat16, device="cuda")
+        self.flops = 2.0 * self.M * self.N * self.K
+        # host copies for the end-to-end leg (pinned)
+        self.h_x = torch.empty_like(self.x, device="cpu").pin_memory()
+        self.h_x.copy_(self.x)
+        self.h_resid = None
+        if self.resid is not None:
+            self.h_resid = torch.empty_like(self.resid, device="cpu").pin_memory()
+            self.h_resid.copy_(self.resid)
+        self.h_out = torch.empty_like(self.out, device="cpu").pin_memory()
+
+    def describe(self):
+        wl = self.d["workload"]
+        return (f"{wl.name}: X bf16 [{self.M},{self.K}] -> NVFP4 (in-run amax), W NVFP4 [{self.N},{self.K}], "
+                f"{wl.description}")
+
+    def quant(self, A):
+        A.h3fp4_quantize_act(self.x, *self.aq, self.ws, shift=self.shift, scale=self.scale, seg_off=self.seg_off)
+
+    def gemm(self, A):
+        A.h3fp4_linear(self.aq[0], *self.wq, self.out, self.ws, a_sf=self.aq[1], a_gscale=self.aq[2],
+                       gate=self.gate, resid=self.resid, bias=self.bias, seg_off=self.seg_off)
+
+    def fused_from_device(self, A, x, resid, out):
+        A.h3fp4_linear(x, *self.wq, out, self.ws, shift=self.shift, scale=self.scale, gate=self.gate,
+                       resid=resid, bias=self.bias, seg_off=self.seg_off)
+
+    def quant_bytes(self):
+        MK = self.M * self.K
+        return {"amax": 2.0 * MK, "pack": 2.0 * MK + 0.5 * MK + MK / 16.0}
+
+    def gemm_bytes(self):
+        MK, NK, MN = self.M * self.K, self.N * self.K, self.M * self.N
+        b = 0.5625 * (MK + NK) + 2.0 * MN
+        if self.resid is not None:
+            b += 2.0 * MN
+        return b
+
+
+def time_device_steps(torch, A, prob: Problem, steps: int, warmup: int, flush):
+    """Per-step CUDA events on the launching stream: [quant | gemm], L2 flushed between steps."""
+    s = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush()
+        prob.quant(A)
+        prob.gemm(A)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    t0 = time.perf_counter()
+    for i in range(steps):
+        flush()
+        ev[i][0].record(s)
+        prob.quant(A)
+        ev[i][1].record(s)
+        prob.gemm(A)
+        ev[i][2].record(s)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    q = np.array([a.elapsed_time(b) for a, b, _ in ev])
+    g = np.array([b.elapsed_time(c) for _, b, c in ev])
+    A.h3fp4_check(prob.ws)
+    return q, g, wall
+
+
+def time_e2e(torch, A, prob: Problem, steps: int, warmup: int):
+    """Public API end to end: pinned host X (+R) -> device, fused h3fp4_linear, output -> host."""
+    s = torch.cuda.current_stream()
+    x = torch.empty_like(prob.x)
+    resid = None if prob.resid is None else torch.empty_like(prob.resid)
+    out = torch.empty_like(prob.out)
+
+    def step():
+        x.copy_(prob.h_x, non_blocking=True)
+        if resid is not None:
+            resid.copy_(prob.h_resid, non_blocking=True)
+        prob.fused_from_device(A, x, resid, out)
+        prob.h_out.copy_(out, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        step()
+    e1.record(s)
+    torch.cuda.synchronize()
+    A.h3fp4_check(prob.ws)
+    ms = e0.elapsed_time(e1) / steps
+    h2d = prob.h_x.numel() * 2 + (0 if prob.h_resid is None else prob.h_resid.numel() * 2)
+    d2h = prob.h_out.numel() * 2
+    return ms, h2d, d2h
+
+
+def oracle_sample(name: str, rows: int):
+    """The CPU oracle, as it stands, on the first `rows` rows of the workload:
+    quantise X (its own amax) and W, then every output of those rows in float64."""
+    import oracle
+    import workloads as W
+    d = W.make_inputs(name, M=rows)
+    t0 = time.perf_counter()
+    a = oracle.quantize(d["x"], d["shift"], d["scale"], d["seg_off"])
+    w = oracle.quantize(d["w"])
+    oracle.linear_full(a, w, rows, d["N"], d["K"], bias=d["bias"], gate=d["gate"], resid=d["resid"],
+                       seg_off=d["seg_off"])
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * d["N"] * d["K"]
+    return flops / dt / 1e12, dt, oracle.num_threads()
+
+
+def run_gpu(args):
+    import torch
+    import audio_dit_gb300 as A
+    from audio_dit_gb300 import build as B
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0 or not os.path.exists(A.library_path()):
+        B.build()
+    if dist is not None:
+        dist.barrier()
+    A.load_library()
+    peaks = load_peaks()
+
+    prob = Problem(args.config, torch, A)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = lambda: flush_buf.fill_(1)
+
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        q, g, wall = time_device_steps(torch, A, prob, args.steps, args.warmup, flush)
+    torch.cuda.synchronize()
+    step_ms = float(np.mean(q + g))
+    if dist is not None:
+        t = torch.tensor([step_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms = float(t.item())
+        dist.barrier()
+    e2e_ms, h2d, d2h = time_e2e(torch, A, prob, max(3, args.steps // 2), args.warmup)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    value = world * prob.flops / (step_ms * 1e-3) / 1e12
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    gemm_ms = float(np.mean(g))
+    gemm_tflops = prob.flops / (gemm_ms * 1e-3) / 1e12
+    qb = prob.quant_bytes()
+    quant_ms = float(np.mean(q))
+    quant_gbs = (qb["amax"] + qb["pack"]) / (quant_ms * 1e-3) / 1e9
+
+    extra = {}
+    if rank == 0 and not args.no_extra:
+        for name in [c for c in ["fc1", "fc2", "attn_out"] if c != args.config]:
+            try:
+                pe = Problem(name, torch, A)
+                qe, ge, _ = time_device_steps(torch, A, pe, max(5, args.steps // 2), 3, flush)
+                qbe = pe.quant_bytes()
+                extra[name] = {
+                    "tflops": round(pe.flops / (np.mean(qe + ge) * 1e-3) / 1e12, 1),
+                    "gemm_tflops": round(pe.flops / (np.mean(ge) * 1e-3) / 1e12, 1),
+                    "gemm_frac_fp4_peak": round(pe.flops / (np.mean(ge) * 1e-3) / 1e12 / fp4_peak, 4),
+                    "quant_gbs": round((qbe["amax"] + qbe["pack"]) / (np.mean(qe) * 1e-3) / 1e9, 1),
+                    "ms_per_step": round(float(np.mean(qe + ge)), 4),
+                }
+                del pe
+                torch.cuda.empty_cache()
+            except Exception as e:  # a failing extra config must not hide the headline
+                extra[name] = {"error": repr(e)[:200]}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rows = args.cpu_rows
+        tf, dt, cores = oracle_sample(args.config, rows)
+        cpu = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+               "sample": f"first {rows} rows of {args.config} (own amax), W quantised, all {rows}x{prob.N} "
+                         f"outputs in float64; {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "TFLOPS",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(step_ms, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "nvfp4 (e2m1 x e2m1, e4m3 block scales, fp32 accumulate)",
+            "data": "synthetic (seeded, shapes/distributions of the workload set)",
+            "config": {"workload": prob.describe(), "M": prob.M, "N": prob.N, "K": prob.K,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)",
+                       "global_scale": "computed in-run (amax pass)"},
+            "e2e": {"value": round(world * prob.flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": 3 * args.steps,
+            "roofline": {"bound": "tensor", "kernel": "nvfp4_gemm_kernel",
+                         "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
+                         "frac": round(gemm_tflops / fp4_peak, 4),
+                         "peak_source": f"{peaks['source']} bf16 burst {peaks['bf16_tflops']} x nominal fp4/bf16 6",
+                         "traffic": None, "algorithmic_bytes": prob.gemm_bytes()},
+            "quant": {"gbs": round(quant_gbs, 1), "peak_gbs": peaks["hbm_gbs"],
+                      "frac": round(quant_gbs / peaks["hbm_gbs"], 4), "ms": round(quant_ms, 5),
+                      "bytes": "amax read 2 B/elem + pack read 2 + codes 0.5 + scales 1/16 B/elem"},
+            "gemm_ms": round(gemm_ms, 5),
+            "clocks": clk.summary(),
+            "wall_s_timed": round(wall, 3),
+        }
+        if extra:
+            line["also"] = extra
+        if cpu:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------- reference arm (oracle)
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import workloads as W
+    import oracle
+    oracle.build()
+    rows = args.cpu_rows
+    for _ in range(args.warmup):
+        oracle_sample(args.config, max(8, rows // 8))
+    vals, times = [], []
+    for _ in range(args.steps):
+        tf, dt, cores = oracle_sample(args.config, rows)
+        vals.append(tf)
+        times.append(dt)
+    wl = W.WORKLOADS[args.config]
+    v = float(np.mean(vals))
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": v,
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": float(np.mean(times)) * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64 (oracle: fp32 quantiser, float64 GEMM)",
+        "data": "synthetic (seeded, shapes/distributions of the workload set)",
+        "config": {"workload": f"{wl.name}: first {rows} rows of X [{wl.M},{wl.K}], W [{wl.N},{wl.K}]",
+                   "M": rows, "N": wl.N, "K": wl.K},
+        "cpu_baseline": {"value": v, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{rows} rows of {wl.name} per step"},
+        "e2e": {"value": v, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=["tiny", "qkv", "fc1", "fc2", "attn_out"])
+    ap.add_argument("--cpu-rows", type=int, default=256)
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
