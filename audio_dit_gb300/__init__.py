@@ -20,7 +20,8 @@ __all__ = [
     "H3FP4Error", "PROLOGUE_MOD", "EPI_BIAS", "EPI_GATE_RESID", "GSCALE_GIVEN", "A_PREQUANT",
     "MAX_SEGMENTS", "library_path", "load_library", "h3fp4_codes_bytes", "h3fp4_sf_bytes",
     "h3fp4_workspace_bytes", "h3fp4_quantize_weight", "h3fp4_quantize_act", "h3fp4_linear",
-    "h3fp4_check", "h3fp4_set_wait_limit_ns", "h3fp4_status_string", "alloc_nvfp4", "alloc_workspace",
+    "h3fp4_check", "h3fp4_act_amax", "h3fp4_gscale_from_amax", "h3fp4_selftest_timeout",
+    "h3fp4_set_wait_limit_ns", "h3fp4_status_string", "alloc_nvfp4", "alloc_workspace",
 ]
 
 PROLOGUE_MOD = 1
@@ -62,6 +63,9 @@ def load_library():
         "h3fp4_quantize_act": (i32, [vp, i64, i64, vp, vp, vp, i32, vp, vp, vp, i32, vp, vp]),
         "h3fp4_linear": (i32, [vp, vp, vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp,
                                i32, vp, vp]),
+        "h3fp4_act_amax": (i32, [vp, i64, i64, vp, vp, vp, i32, vp, i32, vp, vp]),
+        "h3fp4_gscale_from_amax": (i32, [vp, vp, vp]),
+        "h3fp4_selftest_timeout": (i32, [vp, C.c_uint64, vp]),
         "h3fp4_check": (i32, [vp, vp]),
         "h3fp4_set_wait_limit_ns": (None, [C.c_uint64]),
         "h3fp4_status_string": (C.c_char_p, [i32]),
@@ -181,6 +185,30 @@ def h3fp4_linear(x: torch.Tensor, w_codes: torch.Tensor, w_sf: torch.Tensor, w_g
         _ptr(bias, "bias", torch.bfloat16), _ptr(resid, "resid", torch.bfloat16),
         _ptr(out, "out", torch.bfloat16), flags, _ptr(ws, "ws", torch.uint8), _stream(stream)),
         "h3fp4_linear")
+
+
+def h3fp4_act_amax(x: torch.Tensor, amax: torch.Tensor, ws: torch.Tensor, shift: Optional[torch.Tensor] = None,
+                   scale: Optional[torch.Tensor] = None, seg_off: Optional[Sequence[int]] = None,
+                   stream=None) -> None:
+    """amax of this call's (modulated) rows into ``amax`` (device fp32 [1])."""
+    M, K = x.shape
+    sp, nseg, _keep = _segs(seg_off)
+    _check(load_library().h3fp4_act_amax(
+        _ptr(x, "x", torch.bfloat16), M, K, _ptr(shift, "shift", torch.float32),
+        _ptr(scale, "scale", torch.float32), sp, nseg, _ptr(amax, "amax", torch.float32),
+        PROLOGUE_MOD if shift is not None else 0, _ptr(ws, "ws", torch.uint8), _stream(stream)),
+        "h3fp4_act_amax")
+
+
+def h3fp4_gscale_from_amax(amax: torch.Tensor, gscale: torch.Tensor, stream=None) -> None:
+    _check(load_library().h3fp4_gscale_from_amax(_ptr(amax, "amax", torch.float32),
+                                                 _ptr(gscale, "gscale", torch.float32), _stream(stream)),
+           "h3fp4_gscale_from_amax")
+
+
+def h3fp4_selftest_timeout(ws: torch.Tensor, limit_ns: int, stream=None) -> None:
+    _check(load_library().h3fp4_selftest_timeout(_ptr(ws, "ws", torch.uint8), int(limit_ns), _stream(stream)),
+           "h3fp4_selftest_timeout")
 
 
 def h3fp4_check(ws: torch.Tensor, stream=None) -> None:

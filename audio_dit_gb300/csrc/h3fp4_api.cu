@@ -231,6 +231,68 @@ h3fp4_status h3fp4_linear(const void* x, const void* a_sf, const float* a_gscale
     return from_cuda(launch_gemm(g, stream));
 }
 
+h3fp4_status h3fp4_act_amax(const void* x_bf16, int64_t M, int64_t K, const float* shift, const float* scale,
+                            const int64_t* seg_off, int nseg, float* amax, int flags, void* ws, cudaStream_t stream)
+{
+    h3fp4_status st = check_shape(M, K);
+    if (st != H3FP4_OK) return st;
+    if (!x_bf16 || !amax || !ws) return H3FP4_ERR_INVALID;
+    if (flags & ~H3FP4_PROLOGUE_MOD) return H3FP4_ERR_INVALID;
+    const bool mod = (flags & H3FP4_PROLOGUE_MOD) != 0;
+    if (mod && (!shift || !scale)) return H3FP4_ERR_INVALID;
+    if (!aligned16(x_bf16) || !aligned16(ws) || (reinterpret_cast<uintptr_t>(amax) & 3u) ||
+        (mod && (!aligned16(shift) || !aligned16(scale))))
+        return H3FP4_ERR_ALIGN;
+    QuantJob job{};
+    st = make_segments(seg_off, nseg <= 0 ? 1 : nseg, M, &job.seg);
+    if (st != H3FP4_OK) return st;
+    if ((st = check_device()) != H3FP4_OK) return st;
+    job.x = x_bf16;
+    job.rows = M;
+    job.K = K;
+    job.shift = mod ? shift : nullptr;
+    job.scale = mod ? scale : nullptr;
+    job.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWsPartials);
+    return from_cuda(launch_amax(job, amax, stream));
+}
+
+h3fp4_status h3fp4_gscale_from_amax(const float* amax, float* gscale, cudaStream_t stream)
+{
+    if (!amax || !gscale) return H3FP4_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(amax) & 3u) || (reinterpret_cast<uintptr_t>(gscale) & 3u))
+        return H3FP4_ERR_ALIGN;
+    h3fp4_status st = check_device();
+    if (st != H3FP4_OK) return st;
+    return from_cuda(launch_gscale_from_amax(amax, gscale, stream));
+}
+
+h3fp4_status h3fp4_selftest_timeout(void* ws, uint64_t limit_ns, cudaStream_t stream)
+{
+    if (!ws) return H3FP4_ERR_INVALID;
+    if (!aligned16(ws)) return H3FP4_ERR_ALIGN;
+    h3fp4_status st = check_device();
+    if (st != H3FP4_OK) return st;
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    GemmJob g{};
+    // Dummy operands: the tensor maps need valid, aligned addresses but the
+    // disabled producer never issues a copy and no output is ever stored.
+    g.a_codes = wsb + kWsActCodes;
+    g.a_sf = wsb + kWsActCodes;
+    g.a_gscale = reinterpret_cast<const float*>(wsb + kWsActGscale);
+    g.w_codes = wsb + kWsActCodes;
+    g.w_sf = wsb + kWsActCodes;
+    g.w_gscale = reinterpret_cast<const float*>(wsb + kWsActGscale);
+    g.M = 128;
+    g.N = 256;
+    g.K = 256;
+    g.out = wsb + kWsActCodes;
+    g.seg.nseg = 1;
+    g.seg.off[1] = 128;
+    g.status = reinterpret_cast<unsigned int*>(wsb + kWsStatus);
+    g.wait_limit_ns = limit_ns ? limit_ns : 1;
+    return from_cuda(launch_gemm_stall_selftest(g, stream));
+}
+
 h3fp4_status h3fp4_check(void* ws, cudaStream_t stream)
 {
     if (!ws) return H3FP4_ERR_INVALID;

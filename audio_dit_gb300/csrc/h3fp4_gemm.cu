@@ -73,6 +73,7 @@ struct GemmParams {
     Segments seg;
     unsigned int* status;
     unsigned long long wait_ns;
+    int stall;  // self-test: the producer issues nothing, so every consumer wait must time out
 };
 
 __device__ __forceinline__ int segment_of_row(const Segments& s, int r)
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t fills[kStages] = {};
-            for (int tile = blockIdx.x; tile < num_tiles && !s_abort; tile += gridDim.x) {
+            for (int tile = blockIdx.x; tile < num_tiles && !s_abort && !p.stall; tile += gridDim.x) {
                 const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
                 const int sfb_tiles = (2 * nt + 1 < p.n_sf_tiles) ? 2 : 1;
                 for (int kb = 0; kb < p.k_stages; ++kb) {
@@ -391,7 +392,13 @@ bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uin
 
 }  // namespace
 
-cudaError_t launch_gemm(const GemmJob& job, cudaStream_t s)
+static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t s);
+
+cudaError_t launch_gemm(const GemmJob& job, cudaStream_t s) { return launch_gemm_impl(job, 0, s); }
+
+cudaError_t launch_gemm_stall_selftest(const GemmJob& job, cudaStream_t s) { return launch_gemm_impl(job, 1, s); }
+
+static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t s)
 {
     CUtensorMap tmA, tmB, tmOut, tmR;
     const uint64_t kbytes = (uint64_t)job.K / 2;
@@ -424,6 +431,7 @@ cudaError_t launch_gemm(const GemmJob& job, cudaStream_t s)
     p.seg = job.seg;
     p.status = job.status;
     p.wait_ns = job.wait_limit_ns;
+    p.stall = stall;
 
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;

@@ -60,6 +60,16 @@ struct GemmJob {
 
 cudaError_t launch_gemm(const GemmJob& job, cudaStream_t s);
 
+// The same GEMM kernel with its producer disabled: every consumer wait runs out,
+// the kernel records a timeout in the status word and returns (self-test).
+cudaError_t launch_gemm_stall_selftest(const GemmJob& job, cudaStream_t s);
+
+// Global amax of the (modulated) activation into amax_out (device fp32).
+cudaError_t launch_amax(const QuantJob& job, float* amax_out, cudaStream_t s);
+
+// gscale = (amax == 0) ? 1 : amax / (6 * 448), one thread.
+cudaError_t launch_gscale_from_amax(const float* amax, float* gscale, cudaStream_t s);
+
 int sm_count_current_device();
 
 }  // namespace h3fp4

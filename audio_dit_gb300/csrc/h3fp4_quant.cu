@@ -237,9 +237,23 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(QuantParams p)
     }
 }
 
-}  // namespace
+// One CTA: max over the amax partials of pass 1 -> *out (the tensor amax).
+__global__ void __launch_bounds__(kThreads) reduce_partials_kernel(const float* partials, int nparts, float* out)
+{
+    __shared__ float red[kThreads / 32];
+    float m = 0.0f;
+    for (int i = threadIdx.x; i < nparts; i += kThreads) m = fmaxf(m, partials[i]);
+    const float amax = block_reduce_max(m, red);
+    if (threadIdx.x == 0) *out = amax;
+}
 
-cudaError_t launch_quantize(const QuantJob& job, cudaStream_t s)
+__global__ void gscale_from_amax_kernel(const float* amax, float* gscale)
+{
+    const float a = *amax;
+    *gscale = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 2688.0f);
+}
+
+QuantParams make_params(const QuantJob& job, dim3* grid)
 {
     QuantParams p{};
     p.x = static_cast<const uint16_t*>(job.x);
@@ -264,7 +278,16 @@ cudaError_t launch_quantize(const QuantJob& job, cudaStream_t s)
     p.rows_per_cta = (p.rows_per_cta + kRowUnroll - 1) / kRowUnroll * kRowUnroll;
     row_groups = (int)((p.rows_pad + p.rows_per_cta - 1) / p.rows_per_cta);
     p.nparts = col_ctas * row_groups;
-    const dim3 grid(col_ctas, row_groups);
+    *grid = dim3(col_ctas, row_groups);
+    return p;
+}
+
+}  // namespace
+
+cudaError_t launch_quantize(const QuantJob& job, cudaStream_t s)
+{
+    dim3 grid;
+    const QuantParams p = make_params(job, &grid);
     const bool mod = job.shift != nullptr;
 
     if (!job.gscale_given) {
@@ -275,6 +298,24 @@ cudaError_t launch_quantize(const QuantJob& job, cudaStream_t s)
     }
     if (mod) pack_kernel<true><<<grid, kThreads, 0, s>>>(p);
     else pack_kernel<false><<<grid, kThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_amax(const QuantJob& job, float* amax_out, cudaStream_t s)
+{
+    dim3 grid;
+    const QuantParams p = make_params(job, &grid);
+    if (job.shift != nullptr) amax_kernel<true><<<grid, kThreads, 0, s>>>(p);
+    else amax_kernel<false><<<grid, kThreads, 0, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    reduce_partials_kernel<<<1, kThreads, 0, s>>>(p.partials, p.nparts, amax_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gscale_from_amax(const float* amax, float* gscale, cudaStream_t s)
+{
+    gscale_from_amax_kernel<<<1, 1, 0, s>>>(amax, gscale);
     return cudaGetLastError();
 }
 

@@ -146,6 +146,31 @@ H3FP4_API h3fp4_status h3fp4_linear(const void* x, const void* a_sf, const float
                           const void* bias_bf16, const void* resid_bf16, void* out_bf16,
                           int flags, void* ws, cudaStream_t stream);
 
+/* Amax of the (modulated) activation rows of this call -> *amax (device fp32).
+ * Building block of the multi-device split of one activation along M (token
+ * rows, "H3 Runtime Current State", "Distributed Execution": sequence-sharded
+ * execution): every device computes the amax of its rows, the caller
+ * max-reduces the per-device values (one fp32 all-reduce(MAX)), turns the
+ * result into the global scale with h3fp4_gscale_from_amax and quantises its
+ * rows with H3FP4_GSCALE_GIVEN.  The codes and block scales are then
+ * bit-identical to a single-device quantisation of the whole tensor.
+ * Arguments as in h3fp4_quantize_act (flags: H3FP4_PROLOGUE_MOD only). */
+H3FP4_API h3fp4_status h3fp4_act_amax(const void* x_bf16, int64_t M, int64_t K,
+                                      const float* shift, const float* scale,
+                                      const int64_t* seg_off, int nseg,
+                                      float* amax, int flags, void* ws, cudaStream_t stream);
+
+/* *gscale = (*amax == 0) ? 1 : *amax / (6*448), on the device (one thread). */
+H3FP4_API h3fp4_status h3fp4_gscale_from_amax(const float* amax, float* gscale, cudaStream_t stream);
+
+/* Failure-detection self-test: runs the GEMM kernel on a dummy 128x256x256
+ * problem with its TMA producer disabled, so every consumer wait must run out
+ * after limit_ns; the kernel then records the timeout in the status word of
+ * `ws` (h3fp4_workspace_bytes(128, 256, 256, 0) bytes), frees
+ * its TMEM and returns.  h3fp4_check(ws) must afterwards report
+ * H3FP4_ERR_TIMEOUT.  No data is read or written besides the status word. */
+H3FP4_API h3fp4_status h3fp4_selftest_timeout(void* ws, uint64_t limit_ns, cudaStream_t stream);
+
 /* Synchronises `stream`, reads and clears the workspace status word.
  * Returns H3FP4_OK, or H3FP4_ERR_TIMEOUT when a kernel gave up early (a
  * bounded device wait ran out, or shared memory came up misaligned); the
