@@ -20,7 +20,7 @@ __all__ = [
     "H3FP4Error", "PROLOGUE_MOD", "EPI_BIAS", "EPI_GATE_RESID", "GSCALE_GIVEN", "A_PREQUANT",
     "MAX_SEGMENTS", "library_path", "load_library", "h3fp4_codes_bytes", "h3fp4_sf_bytes",
     "h3fp4_workspace_bytes", "h3fp4_quantize_weight", "h3fp4_quantize_act", "h3fp4_linear",
-    "h3fp4_check", "h3fp4_act_amax", "h3fp4_gscale_from_amax", "h3fp4_selftest_timeout",
+    "h3fp4_check", "h3fp4_act_amax", "h3fp4_gscale_from_amax", "h3fp4_selftest_timeout", "h3fp4_measure_fp4_peak",
     "h3fp4_set_wait_limit_ns", "h3fp4_status_string", "alloc_nvfp4", "alloc_workspace",
 ]
 
@@ -66,6 +66,7 @@ def load_library():
         "h3fp4_act_amax": (i32, [vp, i64, i64, vp, vp, vp, i32, vp, i32, vp, vp]),
         "h3fp4_gscale_from_amax": (i32, [vp, vp, vp]),
         "h3fp4_selftest_timeout": (i32, [vp, C.c_uint64, vp]),
+        "h3fp4_measure_fp4_peak": (i32, [i32, vp, vp]),
         "h3fp4_check": (i32, [vp, vp]),
         "h3fp4_set_wait_limit_ns": (None, [C.c_uint64]),
         "h3fp4_status_string": (C.c_char_p, [i32]),
@@ -209,6 +210,14 @@ def h3fp4_gscale_from_amax(amax: torch.Tensor, gscale: torch.Tensor, stream=None
 def h3fp4_selftest_timeout(ws: torch.Tensor, limit_ns: int, stream=None) -> None:
     _check(load_library().h3fp4_selftest_timeout(_ptr(ws, "ws", torch.uint8), int(limit_ns), _stream(stream)),
            "h3fp4_selftest_timeout")
+
+
+def h3fp4_measure_fp4_peak(ws: torch.Tensor, iters: int = 20000) -> float:
+    """Measured FP4 MMA ceiling (TFLOP/s) of the current device (synchronous)."""
+    out = C.c_float(0.0)
+    _check(load_library().h3fp4_measure_fp4_peak(int(iters), C.byref(out), _ptr(ws, "ws", torch.uint8)),
+           "h3fp4_measure_fp4_peak")
+    return float(out.value)
 
 
 def h3fp4_check(ws: torch.Tensor, stream=None) -> None:

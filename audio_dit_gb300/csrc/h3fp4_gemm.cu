@@ -7,12 +7,18 @@
 //               alpha-before-BF16 epilogue; "Implemented And Validated": fused
 //               residual gates).
 //
-// Structure (one persistent CTA per SM, 320 threads, warp-specialised):
+// Structure (one persistent CTA per SM, 352 threads, warp-specialised):
 //   warp 0      TMA producer: A/W code tiles (128-byte swizzle) and the 512-byte
 //               block-scale tiles (plain bulk copies) into a 3-stage ring.
-//   warp 1      TMEM owner + MMA issuer: per stage copies the scale tiles to TMEM
-//               (tcgen05.cp 32x128b.warpx4) and issues four
-//               tcgen05.mma.kind::mxf4nvf4.block_scale (M=128, N=256, K=64).
+//   warp 10     block-scale copier: per landed stage, twelve tcgen05.cp
+//               32x128b.warpx4 of the scale tiles into that stage's TMEM slot,
+//               then a tcgen05.commit on the stage's "scales ready" barrier.
+//               Each copy occupies the tensor pipe for ~60 cycles whatever its
+//               size; issuing them from their own thread lets them overlap the
+//               MMAs instead of serialising behind them on one issuer.
+//   warp 1      TMEM owner + MMA issuer: per stage four
+//               tcgen05.mma.kind::mxf4nvf4.block_scale (M=128, N=256, K=64)
+//               once the stage's scales are in TMEM.
 //   warps 2-9   epilogue: tcgen05.ld the 128x256 fp32 accumulator (each warp 32
 //               rows x 128 columns), release TMEM, then alpha/bias/gate/residual
 //               in fp32, bf16 into a 64-byte-swizzled staging tile and TMA store;
@@ -37,7 +43,8 @@ namespace {
 
 constexpr int BM = 128, BN = 256, BK = 256;
 constexpr int kStages = 3;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
+constexpr int kCopyWarp = 10;
 constexpr int kEpiWarps = 8;
 constexpr uint32_t kABytes = BM * BK / 2;            // 16384
 constexpr uint32_t kBBytes = BN * BK / 2;            // 32768
@@ -119,7 +126,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* acc_empty = acc_full + 1;
     uint64_t* rbar = acc_empty + 1;  // one per epilogue warp
     uint64_t* done_bar = rbar + kEpiWarps;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+    uint64_t* sfready = done_bar + 1;  // [kStages]: the stage's scales are in TMEM
+    uint64_t* cp_done = sfready + kStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cp_done + 1);
     volatile int& s_abort = *reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     if (threadIdx.x == 0) {
@@ -132,6 +141,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(acc_empty, kEpiWarps);
         for (int e = 0; e < kEpiWarps; ++e) mbar_init(&rbar[e], 1);
         mbar_init(done_bar, 1);
+        for (int s = 0; s < kStages; ++s) mbar_init(&sfready[s], 1);
+        mbar_init(cp_done, 1);
         fence_mbarrier_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
@@ -199,21 +210,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 bool ok = true;
                 for (int kb = 0; kb < p.k_stages; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma)) {
+                    if (!mbar_wait(&sfready[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma) ||
+                        !mbar_wait(&full[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const int nk = min(4, p.kb4 - kb * 4);
                     const uint32_t st = smem_u32(smem + stage * kStageBytes);
-                    const uint32_t sfa_s = st + kABytes + kBBytes, sfb_s = sfa_s + kSFABytes;
                     const uint32_t sfa_t = tmem + kSfTmem + stage * kSfTmemPerStage;
                     const uint32_t sfb_t = sfa_t + 16;
-                    for (int j = 0; j < nk; ++j) {
-                        tc_cp_32x128b_warpx4(sfa_t + 4 * j, smem_desc(sfa_s + 512 * j, 0, 128, 0));
-                        tc_cp_32x128b_warpx4(sfb_t + 8 * j, smem_desc(sfb_s + 512 * j, 0, 128, 0));
-                        tc_cp_32x128b_warpx4(sfb_t + 8 * j + 4, smem_desc(sfb_s + 2048 + 512 * j, 0, 128, 0));
-                    }
                     for (int j = 0; j < nk; ++j) {
                         const uint64_t adesc = smem_desc(st + 32 * j, 16, 1024, 2);
                         const uint64_t bdesc = smem_desc(st + kABytes + 32 * j, 16, 1024, 2);
@@ -236,6 +242,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Every issued MMA / copy must finish before TMEM is released.
             tc_commit(done_bar);
             (void)mbar_wait(done_bar, 0u, p.wait_ns, p.status, kStatusTimeoutMma);
+        }
+    } else if (warp == kCopyWarp) {
+        // ---------------------------------------------------------------- block-scale copier
+        // The TMEM slot of a stage is rewritten only after the stage was refilled,
+        // i.e. after the MMAs that read the previous contents committed.
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int tile = blockIdx.x; tile < num_tiles && !s_abort; tile += gridDim.x) {
+                bool ok = true;
+                for (int kb = 0; kb < p.k_stages; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int nk = min(4, p.kb4 - kb * 4);
+                    const uint32_t st = smem_u32(smem + stage * kStageBytes);
+                    const uint32_t sfa_s = st + kABytes + kBBytes, sfb_s = sfa_s + kSFABytes;
+                    const uint32_t sfa_t = tmem + kSfTmem + stage * kSfTmemPerStage;
+                    const uint32_t sfb_t = sfa_t + 16;
+                    for (int j = 0; j < nk; ++j) {
+                        tc_cp_32x128b_warpx4(sfa_t + 4 * j, smem_desc(sfa_s + 512 * j, 0, 128, 0));
+                        tc_cp_32x128b_warpx4(sfb_t + 8 * j, smem_desc(sfb_s + 512 * j, 0, 128, 0));
+                        tc_cp_32x128b_warpx4(sfb_t + 8 * j + 4, smem_desc(sfb_s + 2048 + 512 * j, 0, 128, 0));
+                    }
+                    tc_commit(&sfready[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) {
+                    s_abort = 1;
+                    break;
+                }
+            }
+            // every copy must finish before TMEM is released
+            tc_commit(cp_done);
+            (void)mbar_wait(cp_done, 0u, p.wait_ns, p.status, kStatusTimeoutMma);
         }
     } else {
         // ---------------------------------------------------------------- epilogue

@@ -72,4 +72,7 @@ cudaError_t launch_gscale_from_amax(const float* amax, float* gscale, cudaStream
 
 int sm_count_current_device();
 
+// Synchronous: FP4 MMA loop on every SM, returns TFLOP/s (status word for its bounded wait).
+cudaError_t measure_fp4_peak(int iters, unsigned int* status, float* tflops);
+
 }  // namespace h3fp4

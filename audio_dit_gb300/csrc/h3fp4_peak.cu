@@ -1,0 +1,95 @@
+// Tensor-core ceiling of this device for the instruction the GEMM uses:
+// back-to-back tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X
+// (M=128, N=256, K=64) on every SM, operands resident in shared memory and
+// block scales resident in TMEM, no global traffic.  Used as the measured FP4
+// peak next to the nominal one in roofline reports.
+#include <cstdint>
+
+#include "h3fp4_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace h3fp4 {
+namespace {
+
+constexpr int kPeakSmem = 49152;  // A 16 KB + B 32 KB
+
+__global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, unsigned int* status)
+{
+    extern __shared__ __align__(1024) uint8_t sm[];
+    __shared__ uint64_t bar;
+    __shared__ uint32_t tbase;
+    const int warp = threadIdx.x >> 5;
+    if ((smem_u32(sm) & 1023u) != 0) return;
+    for (int i = threadIdx.x; i < kPeakSmem; i += blockDim.x) sm[i] = (uint8_t)((i * 7 + 3) & 0x77);
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbarrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tbase, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    {  // every block scale = 1.0 (E4M3 0x38) in columns 256..511
+        uint32_t v[32];
+        for (int i = 0; i < 32; ++i) v[i] = 0x38383838u;
+        const uint32_t t = tbase + ((uint32_t)(32 * warp) << 16);
+        for (int c = 256; c < 512; c += 32) tc_st_32x32b_x32(t + c, v);
+        tc_wait_st();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (threadIdx.x == 0) {
+        const uint32_t s = smem_u32(sm);
+        const uint32_t idesc = (1u << 7) | (1u << 10) | (32u << 17) | (8u << 24);  // N=256, M=128
+        for (int i = 0; i < iters; ++i) {
+            const uint32_t j = (uint32_t)(i & 3);
+            mma_mxf4nvf4(tbase, smem_desc(s + 32 * j, 16, 1024, 2), smem_desc(s + 16384 + 32 * j, 16, 1024, 2), idesc,
+                         tbase + 256 + 4 * j, tbase + 320 + 8 * j, i > 0 ? 1u : 0u);
+        }
+        tc_commit(&bar);
+        (void)mbar_wait(&bar, 0u, 2000000000ull, status, kStatusTimeoutMma);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tbase, 512);
+    }
+}
+
+}  // namespace
+
+cudaError_t measure_fp4_peak(int iters, unsigned int* status, float* tflops)
+{
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(mma_peak_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPeakSmem);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    const int sms = sm_count_current_device();
+    cudaEvent_t e0, e1;
+    cudaError_t e = cudaEventCreate(&e0);
+    if (e != cudaSuccess) return e;
+    e = cudaEventCreate(&e1);
+    if (e != cudaSuccess) return e;
+    mma_peak_kernel<<<sms, 128, kPeakSmem>>>(100, status);  // warm-up
+    cudaEventRecord(e0);
+    mma_peak_kernel<<<sms, 128, kPeakSmem>>>(iters, status);
+    cudaEventRecord(e1);
+    e = cudaEventSynchronize(e1);
+    float ms = 0.0f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    if (e != cudaSuccess) return e;
+    *tflops = (float)(2.0 * 128 * 256 * 64 * (double)iters * sms / (ms * 1e-3) / 1e12);
+    return cudaGetLastError();
+}
+
+}  // namespace h3fp4

@@ -32,6 +32,9 @@ METRIC = "fused NVFP4 linear TFLOPS (% GB300 FP4 peak); act-quant GB/s (% HBM), 
 L2_FLUSH_BYTES = 256 << 20
 FP4_OVER_BF16 = 6.0   # nominal dense fp4 / bf16 tensor ratio (13.5 / 2.25 PFLOP/s)
 DEFAULT_CONFIG = "qkv"
+# DRAM bytes (read + write) per launch of nvfp4_gemm_kernel from one ncu capture
+# of the current kernel (profiles/nvfp4_gemm_qkv.md); None where not captured.
+NCU_GEMM_TRAFFIC = {"qkv": 30.186752e6 + 98.243328e6}
 
 
 def load_peaks():
@@ -282,6 +285,7 @@ def run_gpu(args):
 
     value = world * prob.flops / (step_ms * 1e-3) / 1e12
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    mma_peak = A.h3fp4_measure_fp4_peak(prob.ws, 20000) if rank == 0 else None
     gemm_ms = float(np.mean(g))
     gemm_tflops = prob.flops / (gemm_ms * 1e-3) / 1e12
     qb = prob.quant_bytes()
@@ -293,7 +297,7 @@ def run_gpu(args):
         for name in [c for c in ["fc1", "fc2", "attn_out"] if c != args.config]:
             try:
                 pe = Problem(name, torch, A)
-                qe, ge, _ = time_device_steps(torch, A, pe, max(5, args.steps // 2), 3, flush)
+                qe, ge, _ = time_device_steps(torch, A, pe, max(5, min(200, args.steps // 4)), 3, flush)
                 qbe = pe.quant_bytes()
                 extra[name] = {
                     "tflops": round(pe.flops / (np.mean(qe + ge) * 1e-3) / 1e12, 1),
@@ -340,7 +344,9 @@ def run_gpu(args):
                          "achieved": round(gemm_tflops, 1), "peak": round(fp4_peak, 1), "unit": "TFLOP/s",
                          "frac": round(gemm_tflops / fp4_peak, 4),
                          "peak_source": f"{peaks['source']} bf16 burst {peaks['bf16_tflops']} x nominal fp4/bf16 6",
-                         "traffic": None, "algorithmic_bytes": prob.gemm_bytes()},
+                         "measured_mma_peak": round(mma_peak, 1) if mma_peak else None,
+                         "frac_of_measured_mma_peak": round(gemm_tflops / mma_peak, 4) if mma_peak else None,
+                         "traffic": NCU_GEMM_TRAFFIC.get(args.config), "algorithmic_bytes": prob.gemm_bytes()},
             "quant": {"gbs": round(quant_gbs, 1), "peak_gbs": peaks["hbm_gbs"],
                       "frac": round(quant_gbs / peaks["hbm_gbs"], 4), "ms": round(quant_ms, 5),
                       "bytes": "amax read 2 B/elem + pack read 2 + codes 0.5 + scales 1/16 B/elem"},
@@ -404,8 +410,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=["tiny", "qkv", "fc1", "fc2", "attn_out"])
     ap.add_argument("--cpu-rows", type=int, default=256)

@@ -171,6 +171,15 @@ H3FP4_API h3fp4_status h3fp4_gscale_from_amax(const float* amax, float* gscale, 
  * H3FP4_ERR_TIMEOUT.  No data is read or written besides the status word. */
 H3FP4_API h3fp4_status h3fp4_selftest_timeout(void* ws, uint64_t limit_ns, cudaStream_t stream);
 
+/* Measured tensor-core ceiling for the GEMM's instruction on the current
+ * device: back-to-back tcgen05.mma.kind::mxf4nvf4.block_scale (M=128, N=256,
+ * K=64) on every SM with operands resident in shared memory and scales in
+ * TMEM (no global traffic), `iters` MMAs per SM (e.g. 20000).  Synchronous
+ * (default stream); writes TFLOP/s to *tflops.  ws: any workspace (status
+ * word only).  The roofline reports of the benchmark quote this beside the
+ * nominal dense FP4 figure. */
+H3FP4_API h3fp4_status h3fp4_measure_fp4_peak(int iters, float* tflops, void* ws);
+
 /* Synchronises `stream`, reads and clears the workspace status word.
  * Returns H3FP4_OK, or H3FP4_ERR_TIMEOUT when a kernel gave up early (a
  * bounded device wait ran out, or shared memory came up misaligned); the
