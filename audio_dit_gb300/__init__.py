@@ -20,7 +20,7 @@ __all__ = [
     "H3FP4Error", "PROLOGUE_MOD", "EPI_BIAS", "EPI_GATE_RESID", "GSCALE_GIVEN", "A_PREQUANT",
     "MAX_SEGMENTS", "library_path", "load_library", "h3fp4_codes_bytes", "h3fp4_sf_bytes",
     "h3fp4_workspace_bytes", "h3fp4_quantize_weight", "h3fp4_quantize_act", "h3fp4_linear",
-    "h3fp4_check", "h3fp4_act_amax", "h3fp4_gscale_from_amax", "h3fp4_selftest_timeout", "h3fp4_measure_fp4_peak",
+    "h3fp4_check", "h3fp4_act_amax", "h3fp4_gscale_from_amax", "h3fp4_selftest_timeout", "h3fp4_measure_fp4_peak", "h3fp4_quantize_act_noalloc",
     "h3fp4_set_wait_limit_ns", "h3fp4_status_string", "alloc_nvfp4", "alloc_workspace",
 ]
 
@@ -67,6 +67,7 @@ def load_library():
         "h3fp4_gscale_from_amax": (i32, [vp, vp, vp]),
         "h3fp4_selftest_timeout": (i32, [vp, C.c_uint64, vp]),
         "h3fp4_measure_fp4_peak": (i32, [i32, vp, vp]),
+        "h3fp4_quantize_act_noalloc": (i32, [vp, i64, i64, vp, vp, vp, i32, vp, vp, vp, i32, vp]),
         "h3fp4_check": (i32, [vp, vp]),
         "h3fp4_set_wait_limit_ns": (None, [C.c_uint64]),
         "h3fp4_status_string": (C.c_char_p, [i32]),
@@ -186,6 +187,23 @@ def h3fp4_linear(x: torch.Tensor, w_codes: torch.Tensor, w_sf: torch.Tensor, w_g
         _ptr(bias, "bias", torch.bfloat16), _ptr(resid, "resid", torch.bfloat16),
         _ptr(out, "out", torch.bfloat16), flags, _ptr(ws, "ws", torch.uint8), _stream(stream)),
         "h3fp4_linear")
+
+
+def h3fp4_quantize_act_noalloc(x: torch.Tensor, codes: torch.Tensor, sf: torch.Tensor, gscale: torch.Tensor,
+                               shift: Optional[torch.Tensor] = None, scale: Optional[torch.Tensor] = None,
+                               seg_off: Optional[Sequence[int]] = None, gscale_given: bool = False,
+                               stream=None) -> None:
+    """h3fp4_quantize_act without a workspace, for callers that may not allocate
+    device memory; its scratch is a static device array shared by all calls
+    (serialise calls that could overlap on the GPU)."""
+    M, K = x.shape
+    flags = (PROLOGUE_MOD if shift is not None else 0) | (GSCALE_GIVEN if gscale_given else 0)
+    sp, nseg, _keep = _segs(seg_off)
+    _check(load_library().h3fp4_quantize_act_noalloc(
+        _ptr(x, "x", torch.bfloat16), M, K, _ptr(shift, "shift", torch.float32),
+        _ptr(scale, "scale", torch.float32), sp, nseg, _ptr(codes, "codes", torch.uint8),
+        _ptr(sf, "sf", torch.uint8), _ptr(gscale, "gscale", torch.float32), flags, _stream(stream)),
+        "h3fp4_quantize_act_noalloc")
 
 
 def h3fp4_act_amax(x: torch.Tensor, amax: torch.Tensor, ws: torch.Tensor, shift: Optional[torch.Tensor] = None,

@@ -146,6 +146,29 @@ H3FP4_API h3fp4_status h3fp4_linear(const void* x, const void* a_sf, const float
                           const void* bias_bf16, const void* resid_bf16, void* out_bf16,
                           int flags, void* ws, cudaStream_t stream);
 
+/* Quantise an activation exactly like h3fp4_quantize_act, but without a
+ * workspace and without allocating anything, for callers that are handed only
+ * their input and output buffers: for example a plugin whose host application
+ * owns all device memory and gives it no workspace, or a serving loop that
+ * forbids device allocation once it runs (cudaMalloc/cudaFree can synchronise
+ * the device and fragment a pool another allocator manages).  The pages have
+ * no counterpart for this entry point; it is a convenience of this library.
+ *   Scratch: the amax partial maxima live in a static device array of the
+ *   library (4096 fp32 = 16 KiB), held by every GPU that loads the library
+ *   until the process exits.  The first call on a device looks up the array's
+ *   device address (cudaGetSymbolAddress) with that device current; make that
+ *   first call before any stream capture.  All calls share the array: calls
+ *   that can overlap on the GPU (several streams or host threads) race on it
+ *   and must be serialised by the caller.
+ *   Limit: K <= 4096 * 1024 columns (one partial per 1024-column slab at
+ *   least); larger K returns H3FP4_ERR_SHAPE.
+ *   Other arguments, results and errors as in h3fp4_quantize_act. */
+H3FP4_API h3fp4_status h3fp4_quantize_act_noalloc(const void* x_bf16, int64_t M, int64_t K,
+                                                  const float* shift, const float* scale,
+                                                  const int64_t* seg_off, int nseg,
+                                                  void* codes, void* sf, float* gscale,
+                                                  int flags, cudaStream_t stream);
+
 /* Amax of the (modulated) activation rows of this call -> *amax (device fp32).
  * Building block of the multi-device split of one activation along M (token
  * rows, "H3 Runtime Current State", "Distributed Execution": sequence-sharded
