@@ -27,8 +27,8 @@
 namespace h3fp4 {
 namespace {
 
-constexpr int kThreads = 128;
-constexpr int kRowUnroll = 4;
+constexpr int kThreads = 64;     // one 16-element block per thread: 1024 columns per CTA
+constexpr int kRowUnroll = 4;    // rows in flight per thread
 
 struct QuantParams {
     const uint16_t* x;
@@ -48,18 +48,37 @@ struct QuantParams {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// fp32 -> bf16 (round to nearest even) -> fp32: the exact BF16 modulated value.
-__device__ __forceinline__ float round_bf16(float v)
+// Sixteen bf16 values = 32 bytes: one 256-bit load when the row pointer is
+// 32-byte aligned, two 128-bit loads otherwise.
+struct V16 {
+    uint32_t w[8];
+};
+
+template <bool kWide>
+__device__ __forceinline__ V16 ld16(const uint16_t* p)
 {
-    return __bfloat162float(__float2bfloat16_rn(v));
+    V16 v;
+    if (kWide) {
+        asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                     : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]),
+                       "=r"(v.w[6]), "=r"(v.w[7])
+                     : "l"(p));
+    } else {
+        const uint4 a = ld_stream_v4(p);
+        const uint4 b = ld_stream_v4(p + 8);
+        v.w[0] = a.x; v.w[1] = a.y; v.w[2] = a.z; v.w[3] = a.w;
+        v.w[4] = b.x; v.w[5] = b.y; v.w[6] = b.z; v.w[7] = b.w;
+    }
+    return v;
 }
 
-__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8])
+__device__ __forceinline__ void unpack16(const V16& v, float (&f)[16])
 {
-    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
-    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
-    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        f[2 * i] = bf16_lo(v.w[i]);
+        f[2 * i + 1] = bf16_hi(v.w[i]);
+    }
 }
 
 __device__ __forceinline__ int segment_of(const Segments& s, long long r)
@@ -70,26 +89,28 @@ __device__ __forceinline__ int segment_of(const Segments& s, long long r)
     return i;
 }
 
-// Per-thread modulation constants for the 8 columns it owns.
+// Per-thread modulation constants for the 16 columns it owns.
 struct ModCols {
-    float onep[8], sh[8];
+    float onep[16], sh[16];
     long long seg_end;
 };
 
-__device__ __forceinline__ void load_mod(const QuantParams& p, int seg, int cv, ModCols& mc)
+__device__ __forceinline__ void load_mod(const QuantParams& p, int seg, int cb, ModCols& mc)
 {
-    const float* sc = p.scale + (long long)seg * p.K + (long long)cv * 8;
-    const float* sh = p.shift + (long long)seg * p.K + (long long)cv * 8;
-    const float4 a0 = __ldg(reinterpret_cast<const float4*>(sc));
-    const float4 a1 = __ldg(reinterpret_cast<const float4*>(sc) + 1);
-    const float4 b0 = __ldg(reinterpret_cast<const float4*>(sh));
-    const float4 b1 = __ldg(reinterpret_cast<const float4*>(sh) + 1);
-    const float s8[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-    const float h8[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    const float4* sc = reinterpret_cast<const float4*>(p.scale + (long long)seg * p.K + (long long)cb * 16);
+    const float4* sh = reinterpret_cast<const float4*>(p.shift + (long long)seg * p.K + (long long)cb * 16);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        mc.onep[j] = __fadd_rn(1.0f, s8[j]);
-        mc.sh[j] = h8[j];
+    for (int i = 0; i < 4; ++i) {
+        const float4 a = __ldg(sc + i);
+        const float4 b = __ldg(sh + i);
+        mc.onep[4 * i + 0] = __fadd_rn(1.0f, a.x);
+        mc.onep[4 * i + 1] = __fadd_rn(1.0f, a.y);
+        mc.onep[4 * i + 2] = __fadd_rn(1.0f, a.z);
+        mc.onep[4 * i + 3] = __fadd_rn(1.0f, a.w);
+        mc.sh[4 * i + 0] = b.x;
+        mc.sh[4 * i + 1] = b.y;
+        mc.sh[4 * i + 2] = b.z;
+        mc.sh[4 * i + 3] = b.w;
     }
     mc.seg_end = p.seg.off[seg + 1];
 }
@@ -97,19 +118,29 @@ __device__ __forceinline__ void load_mod(const QuantParams& p, int seg, int cv, 
 __device__ __forceinline__ void init_mod(ModCols& mc)
 {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < 16; ++j) {
         mc.onep[j] = 1.0f;
         mc.sh[j] = 0.0f;
     }
     mc.seg_end = -1;
 }
 
+// m = bf16(fma(x, 1 + scale, shift)) for 16 values: one fp32 fma each, then one
+// packed round-to-nearest-even conversion per pair (cvt.rn.bf16x2.f32 rounds
+// each half exactly like the scalar conversion, at half the conversion cost).
 template <bool kMod>
-__device__ __forceinline__ void modulate8(float (&f)[8], const ModCols& mc)
+__device__ __forceinline__ void modulate16(float (&f)[16], const ModCols& mc)
 {
     if (kMod) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) f[j] = round_bf16(__fmaf_rn(f[j], mc.onep[j], mc.sh[j]));
+        for (int j = 0; j < 8; ++j) {
+            const float a = __fmaf_rn(f[2 * j], mc.onep[2 * j], mc.sh[2 * j]);
+            const float b = __fmaf_rn(f[2 * j + 1], mc.onep[2 * j + 1], mc.sh[2 * j + 1]);
+            const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+            const uint32_t u = *reinterpret_cast<const uint32_t*>(&h);
+            f[2 * j] = bf16_lo(u);
+            f[2 * j + 1] = bf16_hi(u);
+        }
     }
 }
 
@@ -129,35 +160,34 @@ __device__ __forceinline__ float block_reduce_max(float v, float* red)
 
 // ------------------------------------------------------------------ pass 1: amax
 
-template <bool kMod>
+template <bool kMod, bool kWide>
 __global__ void __launch_bounds__(kThreads) amax_kernel(QuantParams p)
 {
     __shared__ float red[kThreads / 32];
-    const int cv = blockIdx.x * kThreads + threadIdx.x;
-    const bool valid = cv < p.K / 8;
+    const int cb = blockIdx.x * kThreads + threadIdx.x;  // 16-element block column
+    const bool valid = cb < p.K / 16;
     const long long r0 = (long long)blockIdx.y * p.rows_per_cta;
     const long long r1 = min(r0 + (long long)p.rows_per_cta, p.rows);
-    const uint16_t* xc = p.x + (long long)cv * 8;
+    const uint16_t* xc = p.x + (long long)cb * 16;
 
     ModCols mc;
     init_mod(mc);
     float mx = 0.0f;
-    long long r = r0;
-    for (; r < r1; r += kRowUnroll) {
+    for (long long r = r0; r < r1; r += kRowUnroll) {
         const int n = (int)min((long long)kRowUnroll, r1 - r);
-        uint4 v[kRowUnroll];
+        V16 v[kRowUnroll];
 #pragma unroll
         for (int u = 0; u < kRowUnroll; ++u)
-            if (valid && u < n) v[u] = ld_stream_v4(xc + (r + u) * p.K);
+            if (valid && u < n) v[u] = ld16<kWide>(xc + (r + u) * p.K);
 #pragma unroll
         for (int u = 0; u < kRowUnroll; ++u) {
             if (!(valid && u < n)) continue;
-            if (kMod && r + u >= mc.seg_end) load_mod(p, segment_of(p.seg, r + u), cv, mc);
-            float f[8];
-            unpack8(v[u], f);
-            modulate8<kMod>(f, mc);
+            if (kMod && r + u >= mc.seg_end) load_mod(p, segment_of(p.seg, r + u), cb, mc);
+            float f[16];
+            unpack16(v[u], f);
+            modulate16<kMod>(f, mc);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) mx = fmaxf(mx, fabsf(f[j]));
+            for (int j = 0; j < 16; ++j) mx = fmaxf(mx, fabsf(f[j]));
         }
     }
     const float m = block_reduce_max(mx, red);
@@ -166,7 +196,7 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(QuantParams p)
 
 // ------------------------------------------------------------------ pass 2: pack
 
-template <bool kMod>
+template <bool kMod, bool kWide>
 __global__ void __launch_bounds__(kThreads) pack_kernel(QuantParams p)
 {
     __shared__ float red[kThreads / 32];
@@ -183,53 +213,54 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(QuantParams p)
     }
 
     const int lane = threadIdx.x & 31;
-    const int cv = blockIdx.x * kThreads + threadIdx.x;
-    const int K8 = (int)(p.K / 8);
-    const bool valid = cv < K8;                 // uniform over each 8-lane group
+    const int cb = blockIdx.x * kThreads + threadIdx.x;
+    const bool valid = cb < p.K / 16;            // uniform over each group of 4 lanes
     const long long kb4 = p.K / 64;             // scale tiles per 128 rows
     const long long r0 = (long long)blockIdx.y * p.rows_per_cta;
     const long long r1 = min(r0 + (long long)p.rows_per_cta, p.rows_pad);
-    const uint16_t* xc = p.x + (long long)cv * 8;
-    uint32_t* codes_c = reinterpret_cast<uint32_t*>(p.codes) + cv;  // 4 bytes per 8 elements
-    const long long g = cv >> 3;                // 64-column group = scale word index
+    const uint16_t* xc = p.x + (long long)cb * 16;
+    uint2* codes_c = reinterpret_cast<uint2*>(p.codes) + cb;  // 8 bytes per block
+    const long long g = cb >> 2;                 // 64-column group = scale word index
 
     ModCols mc;
     init_mod(mc);
     for (long long r = r0; r < r1; r += kRowUnroll) {
-        uint4 v[kRowUnroll];
+        V16 v[kRowUnroll];
 #pragma unroll
         for (int u = 0; u < kRowUnroll; ++u) {
-            v[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (valid && r + u < p.rows) v[u] = ld_stream_v4(xc + (r + u) * p.K);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[u].w[i] = 0u;
+            if (valid && r + u < p.rows) v[u] = ld16<kWide>(xc + (r + u) * p.K);
         }
 #pragma unroll
         for (int u = 0; u < kRowUnroll; ++u) {
             const long long rr = r + u;
             if (rr >= r1) break;                   // uniform over the CTA
             const bool real = rr < p.rows;
-            float f[8];
-            unpack8(v[u], f);
+            float f[16];
+            unpack16(v[u], f);
             if (kMod && real) {
-                if (rr >= mc.seg_end && valid) load_mod(p, segment_of(p.seg, rr), cv, mc);
-                modulate8<kMod>(f, mc);
+                if (rr >= mc.seg_end && valid) load_mod(p, segment_of(p.seg, rr), cb, mc);
+                modulate16<kMod>(f, mc);
             }
-            float lmax = 0.0f;
+            float bmax = 0.0f;
 #pragma unroll
-            for (int j = 0; j < 8; ++j) lmax = fmaxf(lmax, fabsf(f[j]));
-            const float bmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, 1));
+            for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, fabsf(f[j]));
             const uint32_t S = real ? cvt_e4m3(__fdiv_rn(__fdiv_rn(bmax, 6.0f), s_g)) : 0u;
             const float eff = __fmul_rn(e4m3_to_f32(S), s_g);
             const float rcp = (eff == 0.0f) ? 0.0f : fminf(__frcp_rn(eff), FLT_MAX);
-            uint32_t word = 0;
+            uint32_t w0 = 0, w1 = 0;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                word |= cvt_e2m1x2(__fmul_rn(f[2 * j], rcp), __fmul_rn(f[2 * j + 1], rcp)) << (8 * j);
-            if (valid && real) codes_c[rr * (p.K / 8)] = word;
-            // gather the four block scales of this 64-column group into lane%8 == 0
-            const uint32_t s1 = __shfl_down_sync(0xffffffffu, S, 2);
-            const uint32_t s2 = __shfl_down_sync(0xffffffffu, S, 4);
-            const uint32_t s3 = __shfl_down_sync(0xffffffffu, S, 6);
-            if (valid && (lane & 7) == 0) {
+            for (int j = 0; j < 4; ++j) {
+                w0 |= cvt_e2m1x2(__fmul_rn(f[2 * j], rcp), __fmul_rn(f[2 * j + 1], rcp)) << (8 * j);
+                w1 |= cvt_e2m1x2(__fmul_rn(f[8 + 2 * j], rcp), __fmul_rn(f[9 + 2 * j], rcp)) << (8 * j);
+            }
+            if (valid && real) codes_c[rr * (p.K / 16)] = make_uint2(w0, w1);
+            // gather the four block scales of this 64-column group into lane%4 == 0
+            const uint32_t s1 = __shfl_down_sync(0xffffffffu, S, 1);
+            const uint32_t s2 = __shfl_down_sync(0xffffffffu, S, 2);
+            const uint32_t s3 = __shfl_down_sync(0xffffffffu, S, 3);
+            if (valid && (lane & 3) == 0) {
                 const long long off = (((rr >> 7) * kb4 + g) << 9) + ((rr & 31) << 4) + (((rr >> 5) & 3) << 2);
                 *reinterpret_cast<uint32_t*>(p.sf + off) = S | (s1 << 8) | (s2 << 16) | (s3 << 24);
             }
@@ -269,8 +300,17 @@ QuantParams make_params(const QuantJob& job, dim3* grid)
     p.gscale_given = job.gscale_given ? 1 : 0;
     p.partials = job.partials;
 
-    const int col_ctas = (int)((job.K / 8 + kThreads - 1) / kThreads);
-    const int target = sm_count_current_device() * 8;
+    const int col_ctas = (int)((job.K / 16 + kThreads - 1) / kThreads);
+    // One full wave of resident CTAs (the slowest variant's occupancy), each
+    // walking a contiguous range of rows: no half-empty second wave.
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        int a = 0, b = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, pack_kernel<true, true>, kThreads, 0);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, amax_kernel<true, true>, kThreads, 0);
+        per_sm = max(1, min(a, b));
+    }
+    const int target = sm_count_current_device() * per_sm;
     int row_groups = (target + col_ctas - 1) / col_ctas;
     row_groups = max(1, min(row_groups, kMaxPartials / col_ctas));
     // rows per CTA covers the padded rows so the pack pass zeroes scale padding
@@ -282,6 +322,23 @@ QuantParams make_params(const QuantJob& job, dim3* grid)
     return p;
 }
 
+// Row starts are 32-byte aligned when the base is (K % 64 == 0).
+bool wide_ok(const void* x) { return (reinterpret_cast<uintptr_t>(x) & 31u) == 0; }
+
+template <bool kMod>
+void launch_amax_t(const QuantParams& p, dim3 grid, bool wide, cudaStream_t s)
+{
+    if (wide) amax_kernel<kMod, true><<<grid, kThreads, 0, s>>>(p);
+    else amax_kernel<kMod, false><<<grid, kThreads, 0, s>>>(p);
+}
+
+template <bool kMod>
+void launch_pack_t(const QuantParams& p, dim3 grid, bool wide, cudaStream_t s)
+{
+    if (wide) pack_kernel<kMod, true><<<grid, kThreads, 0, s>>>(p);
+    else pack_kernel<kMod, false><<<grid, kThreads, 0, s>>>(p);
+}
+
 }  // namespace
 
 cudaError_t launch_quantize(const QuantJob& job, cudaStream_t s)
@@ -289,15 +346,15 @@ cudaError_t launch_quantize(const QuantJob& job, cudaStream_t s)
     dim3 grid;
     const QuantParams p = make_params(job, &grid);
     const bool mod = job.shift != nullptr;
-
+    const bool wide = wide_ok(job.x);
     if (!job.gscale_given) {
-        if (mod) amax_kernel<true><<<grid, kThreads, 0, s>>>(p);
-        else amax_kernel<false><<<grid, kThreads, 0, s>>>(p);
+        if (mod) launch_amax_t<true>(p, grid, wide, s);
+        else launch_amax_t<false>(p, grid, wide, s);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    if (mod) pack_kernel<true><<<grid, kThreads, 0, s>>>(p);
-    else pack_kernel<false><<<grid, kThreads, 0, s>>>(p);
+    if (mod) launch_pack_t<true>(p, grid, wide, s);
+    else launch_pack_t<false>(p, grid, wide, s);
     return cudaGetLastError();
 }
 
@@ -305,8 +362,8 @@ cudaError_t launch_amax(const QuantJob& job, float* amax_out, cudaStream_t s)
 {
     dim3 grid;
     const QuantParams p = make_params(job, &grid);
-    if (job.shift != nullptr) amax_kernel<true><<<grid, kThreads, 0, s>>>(p);
-    else amax_kernel<false><<<grid, kThreads, 0, s>>>(p);
+    if (job.shift != nullptr) launch_amax_t<true>(p, grid, wide_ok(job.x), s);
+    else launch_amax_t<false>(p, grid, wide_ok(job.x), s);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     reduce_partials_kernel<<<1, kThreads, 0, s>>>(p.partials, p.nparts, amax_out);
