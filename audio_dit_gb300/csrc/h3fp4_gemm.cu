@@ -7,27 +7,43 @@
 //               alpha-before-BF16 epilogue; "Implemented And Validated": fused
 //               residual gates).
 //
-// Structure (one persistent CTA per SM, 352 threads, warp-specialised):
-//   warp 0      TMA producer: A/W code tiles (128-byte swizzle) and the 512-byte
-//               block-scale tiles (plain bulk copies) into a 3-stage ring.
-//   warp 10     block-scale copier: per landed stage, twelve tcgen05.cp
-//               32x128b.warpx4 of the scale tiles into that stage's TMEM slot,
-//               then a tcgen05.commit on the stage's "scales ready" barrier.
-//               Each copy occupies the tensor pipe for ~60 cycles whatever its
-//               size; issuing them from their own thread lets them overlap the
-//               MMAs instead of serialising behind them on one issuer.
-//   warp 1      TMEM owner + MMA issuer: per stage four
-//               tcgen05.mma.kind::mxf4nvf4.block_scale (M=128, N=256, K=64)
-//               once the stage's scales are in TMEM.
-//   warps 2-9   epilogue: tcgen05.ld the 128x256 fp32 accumulator (each warp 32
-//               rows x 128 columns), release TMEM, then alpha/bias/gate/residual
-//               in fp32, bf16 into a 64-byte-swizzled staging tile and TMA store;
-//               the residual tile is TMA-loaded into the same staging buffer
-//               ahead of time.
+// CTA pairs.  The kernel runs as clusters of two CTAs on two SMs; a pair owns
+// a 256 x 256 output tile.  CTA r of the pair loads the 128 rows
+// [m0 + 128 r, +128) of A and the 128 rows [n0 + 128 r, +128) of W, and the
+// leader CTA issues tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 64): each
+// SM's tensor core multiplies its own 128 rows of A by all 256 rows of W,
+// fetching the other half of W from its partner.  Compared with one CTA per
+// 128 x 256 tile this cuts the bytes each SM pulls from L2 per MMA by 30 %
+// (A 4 KB + W 4 KB + scales 1.5 KB instead of 4 + 8 + 1.5 KB) and halves the
+// number of block-scale copies per flop (one paired copy fills both SMs).
 //
-// Tile 128 x 256 x 256 (K in elements).  TMEM: accumulator in columns
-// [0, 256); stage s scale slots at 256 + 48 s (16 columns for A's four 64-K
-// groups, 32 for W's two 128-row halves).  Every mbarrier wait is bounded.
+// Block scales reach TMEM through registers.  The MMA reads the scales of
+// every row of W from all four TMEM lane quarters, so each quarter holds its
+// own copy.  tcgen05.cp (one copy per instruction, ~one instruction per MMA
+// duration while MMAs run) cannot keep up with three scale tiles per MMA;
+// tcgen05.st from registers writes TMEM at ~190 B/clk without slowing the MMAs.
+// So four "scale warps", one per lane quarter, load each stage's 512-byte
+// scale tiles from shared memory and store them into their quarter.
+//
+// Roles (512 threads per CTA in four warpgroups, persistent over pair tiles):
+//   warp 0      TMA producer (both CTAs): A / W code tiles (128-byte swizzle)
+//               complete on the LEADER's "full" barrier of the stage; this
+//               CTA's block-scale tiles complete on its own "scales landed"
+//               barrier (4-stage ring).
+//   warp 1      TMEM owner (both) + MMA issuer (leader): per stage, once both
+//               CTAs' scales are in TMEM, four paired MMAs, then a commit
+//               multicast to both CTAs' "empty" barrier.
+//   warps 4-7   scale warps (both), warp 4 + q serving lane quarter q: per
+//               stage twelve 16-byte shared loads per lane, tcgen05.st of 48
+//               columns, then an arrival on the leader's "scales ready".
+//   warps 8-15  epilogue (both): tcgen05.ld the CTA's 128 x 256 fp32
+//               accumulator (each warp 32 rows x 128 columns), release it to
+//               the leader, then alpha/bias/gate/residual in fp32, bf16 into a
+//               64-byte-swizzled staging tile and TMA store; the residual tile
+//               is TMA-loaded into the same staging buffer ahead of time.
+// Registers per thread (setmaxnreg): warpgroup 0: 40, scale warps: 96,
+// epilogue: 184 (40 + 96 + 2 x 184 = 504 <= 512 x 128 / 128 launched).
+//
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
@@ -41,18 +57,25 @@
 namespace h3fp4 {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 256;
-constexpr int kStages = 3;
-constexpr int kThreads = 352;
-constexpr int kCopyWarp = 10;
+constexpr int BM = 128;                               // rows of A per CTA (256 per pair)
+constexpr int BN = 256;                               // rows of W per pair tile
+constexpr int BK = 256;                               // K elements per stage
+constexpr int kStages = 4;
+constexpr int kThreads = 512;
+constexpr int kScaleWarp0 = 4;   // warps 4..7: scale warps, lane quarter = warp & 3
+constexpr int kEpiWarp0 = 8;     // warps 8..15: epilogue
 constexpr int kEpiWarps = 8;
-constexpr uint32_t kABytes = BM * BK / 2;            // 16384
-constexpr uint32_t kBBytes = BN * BK / 2;            // 32768
-constexpr uint32_t kSFABytes = BM * (BK / 16);       // 2048: four 512-byte tiles
-constexpr uint32_t kSFBBytes = BN * (BK / 16);       // 4096: two rows of four tiles
-constexpr uint32_t kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;
-constexpr uint32_t kChunkBytes = 32 * 32 * 2;        // 32 rows x 32 bf16
-constexpr uint32_t kEpiWarpBytes = 4 * kChunkBytes;  // 8192
+constexpr uint32_t kRegsCtl = 40, kRegsScale = 96, kRegsEpi = 184;
+static_assert(128 * (kRegsCtl + kRegsScale + 2 * kRegsEpi) <= 65536, "setmaxnreg shares exceed the launch budget");
+constexpr uint32_t kABytes = BM * BK / 2;             // 16384
+constexpr uint32_t kBBytes = (BN / 2) * BK / 2;       // 16384: this CTA's half of W
+constexpr uint32_t kSFABytes = BM * (BK / 16);        // 2048: four 512-byte tiles
+constexpr uint32_t kSFBBytes = BN * (BK / 16);        // 4096: both halves, four tiles each
+constexpr uint32_t kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;  // 38912
+constexpr uint32_t kPairTxBytes = 2 * (kABytes + kBBytes);  // both CTAs' code tiles complete on the leader
+constexpr uint32_t kSfBox = 2048;                     // scale-tile TMA box: 8 rows x 256 bytes
+constexpr uint32_t kChunkBytes = 32 * 32 * 2;         // 32 rows x 32 bf16
+constexpr uint32_t kEpiWarpBytes = 4 * kChunkBytes;   // 8192
 constexpr uint32_t kEpiOff = kStages * kStageBytes;
 constexpr uint32_t kBarOff = kEpiOff + kEpiWarps * kEpiWarpBytes;
 constexpr uint32_t kSmemBytes = kBarOff + 256;  // barriers, TMEM address, abort flag
@@ -61,21 +84,21 @@ constexpr uint32_t kSfTmem = 256;
 constexpr uint32_t kSfTmemPerStage = 48;
 static_assert(kSfTmem + kStages * kSfTmemPerStage <= kTmemCols, "TMEM budget");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kStageBytes % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+static_assert(kSFABytes == kSfBox && kSFBBytes == 2 * kSfBox, "scale tiles move in 2 KB boxes");
 
 // Instruction descriptor, kind::mxf4nvf4: A/B E2M1 (1) in bits 7-9 / 10-12,
 // K-major A and B, N >> 3 in bits 17-22, UE4M3 scales (bit 23 = 0),
-// M >> 4 in bits 24-28, scale-factor ids 0, dense K = 64.
-constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+// M >> 4 in bits 24-28 (M = 256: the pair), scale-factor ids 0, dense K = 64.
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(2 * BM >> 4) << 24);
 
 struct GemmParams {
-    const uint8_t* a_sf;
-    const uint8_t* w_sf;
     const float* a_gscale;
     const float* w_gscale;
     const __nv_bfloat16* bias;
     const float* gate;
     int M, N, K;
-    int m_tiles, n_tiles, k_stages, kb4, n_sf_tiles;
+    int m_tiles, n_tiles, pair_m_tiles, k_stages, kb4;
     int has_resid;
     Segments seg;
     unsigned int* status;
@@ -108,27 +131,31 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 
 __global__ void __launch_bounds__(kThreads, 1)
     nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                       const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmR,
                       const GemmParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // Swizzled TMA tiles need 1024-byte alignment; refuse to run otherwise.
+    // Swizzled TMA tiles need 1024-byte alignment; refuse to run otherwise.  Both
+    // CTAs of a pair have the same layout, so both leave here together.
     if ((smem_u32(smem) & 1023u) != 0) {
         if (threadIdx.x == 0) atomicOr(p.status, kStatusBadSmemAlign);
         return;
     }
 
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
-    uint64_t* empty = full + kStages;
-    uint64_t* acc_full = empty + kStages;
-    uint64_t* acc_empty = acc_full + 1;
-    uint64_t* rbar = acc_empty + 1;  // one per epilogue warp
+    const uint32_t rank = cluster_ctarank();  // 0 = leader (issues the MMAs)
+    const bool leader = rank == 0;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);  // leader's: both CTAs' code tiles
+    uint64_t* empty = full + kStages;                                // both: the MMAs released the stage
+    uint64_t* sf_full = empty + kStages;                             // both: this CTA's scale tiles landed
+    uint64_t* sfready = sf_full + kStages;                           // leader's: both CTAs' scales in TMEM
+    uint64_t* acc_full = sfready + kStages;                          // both: accumulator complete
+    uint64_t* acc_empty = acc_full + 1;                              // leader's: both epilogues drained
+    uint64_t* rbar = acc_empty + 1;                                  // one per epilogue warp
     uint64_t* done_bar = rbar + kEpiWarps;
-    uint64_t* sfready = done_bar + 1;  // [kStages]: the stage's scales are in TMEM
-    uint64_t* cp_done = sfready + kStages;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cp_done + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
     volatile int& s_abort = *reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     if (threadIdx.x == 0) {
@@ -136,54 +163,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sf_full[s], 1);
+            mbar_init(&sfready[s], 2 * 4);  // four scale warps in each CTA
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, kEpiWarps);
+        mbar_init(acc_empty, 2 * kEpiWarps);
         for (int e = 0; e < kEpiWarps; ++e) mbar_init(&rbar[e], 1);
         mbar_init(done_bar, 1);
-        for (int s = 0; s < kStages; ++s) mbar_init(&sfready[s], 1);
-        mbar_init(cp_done, 1);
         fence_mbarrier_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        prefetch_tensormap(&tmSFA);
+        prefetch_tensormap(&tmSFB);
         prefetch_tensormap(&tmOut);
         if (p.has_resid) prefetch_tensormap(&tmR);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_slot, kTmemCols);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync();  // both CTAs' barriers and TMEM exist before any cross-CTA traffic
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int num_tiles = p.m_tiles * p.n_tiles;
+    const int num_tiles = p.pair_m_tiles * p.n_tiles;
+    // A timeout anywhere stops both CTAs of the pair.
+    auto set_abort = [&]() {
+        s_abort = 1;
+        st_shared_cluster_u32(mapa_shared(smem_u32((const void*)&s_abort), cluster_ctarank() ^ 1u), 1u);
+    };
 
-    if (warp == 0) {
-        // ---------------------------------------------------------------- producer
-        if (lane == 0) {
+    if (warp < kScaleWarp0) {
+        setmaxnreg_dec<kRegsCtl>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------------------ producer (both CTAs)
+            const uint32_t full_leader = mapa_shared(smem_u32(full), 0);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t fills[kStages] = {};
-            for (int tile = blockIdx.x; tile < num_tiles && !s_abort && !p.stall; tile += gridDim.x) {
-                const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
-                const int sfb_tiles = (2 * nt + 1 < p.n_sf_tiles) ? 2 : 1;
+            for (int tile = blockIdx.x >> 1; tile < num_tiles && !s_abort && !p.stall; tile += gridDim.x >> 1) {
+                const int mp = tile / p.n_tiles, nt = tile - mp * p.n_tiles;
+                const int mt = 2 * mp + (int)rank;  // this CTA's 128-row tile of A
                 for (int kb = 0; kb < p.k_stages; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, p.wait_ns, p.status, kStatusTimeoutProducer)) {
-                        s_abort = 1;
+                        set_abort();
                         break;
                     }
-                    const int nk = min(4, p.kb4 - kb * 4);
                     uint8_t* st = smem + stage * kStageBytes;
-                    const uint32_t bytes = kABytes + kBBytes + (uint32_t)(nk * 512) * (1 + sfb_tiles);
-                    mbar_arrive_expect_tx(&full[stage], bytes);
-                    tma_load_2d(st, &tmA, &full[stage], kb * (BK / 2), mt * BM);
-                    tma_load_2d(st + kABytes, &tmB, &full[stage], kb * (BK / 2), nt * BN);
-                    bulk_load(st + kABytes + kBBytes, p.a_sf + ((size_t)mt * p.kb4 + kb * 4) * 512, nk * 512,
-                              &full[stage]);
-                    for (int j = 0; j < sfb_tiles; ++j)
-                        bulk_load(st + kABytes + kBBytes + kSFABytes + j * 2048,
-                                  p.w_sf + ((size_t)(2 * nt + j) * p.kb4 + kb * 4) * 512, nk * 512, &full[stage]);
+                    const uint32_t bar = full_leader + 8u * (uint32_t)stage;
+                    if (leader) mbar_arrive_expect_tx(&full[stage], kPairTxBytes);
+                    tma_load_2d_pair(st, &tmA, bar, kb * (BK / 2), mt * BM);
+                    tma_load_2d_pair(st + kABytes, &tmB, bar, kb * (BK / 2), nt * BN + (int)rank * (BN / 2));
+                    // Scale tiles as rows of 256 bytes (a 512-byte tile is two rows).
+                    mbar_arrive_expect_tx(&sf_full[stage], kSFABytes + kSFBBytes);
+                    uint8_t* sf = st + kABytes + kBBytes;
+                    tma_load_2d(sf, &tmSFA, &sf_full[stage], 0, (mt * p.kb4 + kb * 4) * 2);
+                    tma_load_2d(sf + kSFABytes, &tmSFB, &sf_full[stage], 0, ((2 * nt) * p.kb4 + kb * 4) * 2);
+                    tma_load_2d(sf + kSFABytes + kSfBox, &tmSFB, &sf_full[stage], 0,
+                                ((2 * nt + 1) * p.kb4 + kb * 4) * 2);
                     ++fills[stage];
                     if (++stage == kStages) {
                         stage = 0;
@@ -191,20 +229,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // Drain: every issued copy must land before the CTA may exit.  The last
-            // fill of stage s completes phase fills[s] - 1 of full[s].
+            // Drain: every copy into either CTA must land before the pair may exit.
+            // The leader's "full" phase of a fill completes only when both CTAs'
+            // code tiles arrived; the last fill of stage s completes phase fills[s] - 1.
             for (int s = 0; s < kStages; ++s)
-                if (fills[s] > 0)
-                    (void)mbar_wait(&full[s], (fills[s] - 1u) & 1u, p.wait_ns, p.status, kStatusTimeoutProducer);
-        }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+                if (fills[s] > 0) {
+                    if (leader)
+                        (void)mbar_wait(&full[s], (fills[s] - 1u) & 1u, p.wait_ns, p.status, kStatusTimeoutProducer);
+                    (void)mbar_wait(&sf_full[s], (fills[s] - 1u) & 1u, p.wait_ns, p.status, kStatusTimeoutProducer);
+                }
+        } else if (warp == 1 && leader && lane == 0) {
+            // ------------------------------------------------------------ MMA issuer (leader)
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
-            for (int tile = blockIdx.x; tile < num_tiles && !s_abort; tile += gridDim.x) {
+            for (int tile = blockIdx.x >> 1; tile < num_tiles && !s_abort; tile += gridDim.x >> 1) {
                 if (!mbar_wait(acc_empty, acc_phase ^ 1u, p.wait_ns, p.status, kStatusTimeoutMma)) {
-                    s_abort = 1;
+                    set_abort();
                     break;
                 }
                 tc_fence_after();
@@ -223,80 +263,103 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < nk; ++j) {
                         const uint64_t adesc = smem_desc(st + 32 * j, 16, 1024, 2);
                         const uint64_t bdesc = smem_desc(st + kABytes + 32 * j, 16, 1024, 2);
-                        mma_mxf4nvf4(tmem, adesc, bdesc, kIdesc, sfa_t + 4 * j, sfb_t + 8 * j,
-                                     (kb > 0 || j > 0) ? 1u : 0u);
+                        mma_pair_mxf4nvf4(tmem, adesc, bdesc, kIdesc, sfa_t + 4 * j, sfb_t + 8 * j,
+                                          (kb > 0 || j > 0) ? 1u : 0u);
                     }
-                    tc_commit(&empty[stage]);
+                    tc_commit_pair_mc(&empty[stage], 3);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) {
-                    s_abort = 1;
+                    set_abort();
                     break;
                 }
-                tc_commit(acc_full);
+                tc_commit_pair_mc(acc_full, 3);
                 acc_phase ^= 1u;
             }
-            // Every issued MMA / copy must finish before TMEM is released.
-            tc_commit(done_bar);
+            // Every issued MMA must finish before TMEM is released.
+            tc_commit_pair(done_bar);
             (void)mbar_wait(done_bar, 0u, p.wait_ns, p.status, kStatusTimeoutMma);
         }
-    } else if (warp == kCopyWarp) {
-        // ---------------------------------------------------------------- block-scale copier
+    } else if (warp < kEpiWarp0) {
+        // ---------------------------------------------------------------- scale warps (both CTAs)
+        // Lane i of the warp for quarter q writes TMEM lane 32 q + i: columns
+        // [sfa_t + 4 j, +4) <- bytes [16 i, 16 i + 16) of A's scale tile for K group j,
+        // columns [sfb_t + 8 j + 4 h, +4) <- the same bytes of W's tile (half h, group j)
+        // -- the TMEM image the MMA reads (each quarter a full copy).
         // The TMEM slot of a stage is rewritten only after the stage was refilled,
         // i.e. after the MMAs that read the previous contents committed.
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            for (int tile = blockIdx.x; tile < num_tiles && !s_abort; tile += gridDim.x) {
-                bool ok = true;
-                for (int kb = 0; kb < p.k_stages; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const int nk = min(4, p.kb4 - kb * 4);
-                    const uint32_t st = smem_u32(smem + stage * kStageBytes);
-                    const uint32_t sfa_s = st + kABytes + kBBytes, sfb_s = sfa_s + kSFABytes;
-                    const uint32_t sfa_t = tmem + kSfTmem + stage * kSfTmemPerStage;
-                    const uint32_t sfb_t = sfa_t + 16;
-                    for (int j = 0; j < nk; ++j) {
-                        tc_cp_32x128b_warpx4(sfa_t + 4 * j, smem_desc(sfa_s + 512 * j, 0, 128, 0));
-                        tc_cp_32x128b_warpx4(sfb_t + 8 * j, smem_desc(sfb_s + 512 * j, 0, 128, 0));
-                        tc_cp_32x128b_warpx4(sfb_t + 8 * j + 4, smem_desc(sfb_s + 2048 + 512 * j, 0, 128, 0));
-                    }
-                    tc_commit(&sfready[stage]);
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
-                }
-                if (!ok) {
-                    s_abort = 1;
+        setmaxnreg_dec<kRegsScale>();
+        const uint32_t q = (uint32_t)(warp & 3);
+        const uint32_t ready_leader = mapa_shared(smem_u32(sfready), 0);
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int tile = blockIdx.x >> 1; tile < num_tiles; tile += gridDim.x >> 1) {
+            bool ok = true;
+            for (int kb = 0; kb < p.k_stages; ++kb) {
+                if (__any_sync(0xffffffffu, s_abort != 0)) {
+                    ok = false;
                     break;
                 }
+                ok = mbar_wait(&sf_full[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sfa_s = smem_u32(smem + stage * kStageBytes + kABytes + kBBytes) + 16u * (uint32_t)lane;
+                const uint32_t sfb_s = sfa_s + kSFABytes;
+                uint32_t va[16], vb[32];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 a = ld_shared_v4(sfa_s + 512u * j);
+                    va[4 * j] = a.x;
+                    va[4 * j + 1] = a.y;
+                    va[4 * j + 2] = a.z;
+                    va[4 * j + 3] = a.w;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 b = ld_shared_v4(sfb_s + kSfBox * h + 512u * j);
+                        vb[8 * j + 4 * h] = b.x;
+                        vb[8 * j + 4 * h + 1] = b.y;
+                        vb[8 * j + 4 * h + 2] = b.z;
+                        vb[8 * j + 4 * h + 3] = b.w;
+                    }
+                }
+                const uint32_t sfa_t = tmem + ((32u * q) << 16) + kSfTmem + stage * kSfTmemPerStage;
+                tc_st_32x32b_x16(sfa_t, va);
+                tc_st_32x32b_x32(sfa_t + 16, vb);
+                tc_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(ready_leader + 8u * (uint32_t)stage);
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
             }
-            // every copy must finish before TMEM is released
-            tc_commit(cp_done);
-            (void)mbar_wait(cp_done, 0u, p.wait_ns, p.status, kStatusTimeoutMma);
+            if (!ok) {
+                if (lane == 0) set_abort();
+                break;
+            }
         }
     } else {
-        // ---------------------------------------------------------------- epilogue
-        const int e = warp - 2;            // 0..7
+        // ---------------------------------------------------------------- epilogue (both CTAs)
+        setmaxnreg_inc<kRegsEpi>();
+        const int e = warp - kEpiWarp0;    // 0..7
         const int q = warp & 3;            // TMEM lane quarter this warp may access
         const int h = e >> 2;              // column half of the 256-wide tile
         uint8_t* stg = smem + kEpiOff + e * kEpiWarpBytes;
         const float alpha = __fmul_rn(__ldg(p.a_gscale), __ldg(p.w_gscale));
         uint32_t acc_phase = 0, r_phase = 0;
         bool r_pending = false;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        for (int tile = blockIdx.x >> 1; tile < num_tiles; tile += gridDim.x >> 1) {
             if (__any_sync(0xffffffffu, s_abort != 0)) break;  // warp-uniform exit
-            const int mt = tile / p.n_tiles, nt = tile - mt * p.n_tiles;
-            const int m0 = mt * BM + 32 * q;      // first row of this warp
-            const int nc0 = nt * BN + 128 * h;    // first column of this warp
+            const int mp = tile / p.n_tiles, nt = tile - mp * p.n_tiles;
+            // (blockIdx.x & 1 is the CTA's rank in its pair)
+            const int m0 = (2 * mp + (int)(blockIdx.x & 1u)) * BM + 32 * q;  // first row of this warp
+            const int nc0 = nt * BN + 128 * h;                                 // first column of this warp
             if (lane == 0) bulk_wait_read_all();  // staging buffer free again
             __syncwarp();
             if (p.has_resid && lane == 0) {
@@ -306,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             r_pending = p.has_resid != 0;
             bool ok = mbar_wait(acc_full, acc_phase, p.wait_ns, p.status, kStatusTimeoutEpilogue);
             if (!__all_sync(0xffffffffu, ok)) {
-                s_abort = 1;
+                if (lane == 0) set_abort();
                 break;
             }
             acc_phase ^= 1u;
@@ -318,12 +381,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);   // accumulator may be overwritten now
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty), 0));  // accumulator free
 
             if (p.has_resid) {
                 ok = mbar_wait(&rbar[e], r_phase, p.wait_ns, p.status, kStatusTimeoutEpilogue);
                 if (!__all_sync(0xffffffffu, ok)) {
-                    s_abort = 1;
+                    if (lane == 0) set_abort();
                     break;
                 }
                 r_phase ^= 1u;
@@ -394,12 +457,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------------------------------------------------------- teardown
+    // No CTA of the pair may release TMEM or exit while the leader's MMAs and
+    // copies can still touch its shared memory or TMEM, or while its partner may
+    // still arrive on its barriers.
     tc_fence_before();
     __syncthreads();
+    cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc_pair(tmem, kTmemCols);
     }
+    cluster_sync();
 }
 
 // ------------------------------------------------------------------ host side
@@ -444,14 +512,52 @@ cudaError_t launch_gemm(const GemmJob& job, cudaStream_t s) { return launch_gemm
 
 cudaError_t launch_gemm_stall_selftest(const GemmJob& job, cudaStream_t s) { return launch_gemm_impl(job, 1, s); }
 
+// Largest number of CTA pairs that can be resident at once on the current
+// device (GPCs with an odd number of free SMs leave one SM idle), cached per device.
+static int max_pairs_current_device()
+{
+    static std::mutex mu;
+    static int cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * (unsigned)sm_count_current_device());
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel, &cfg) != cudaSuccess || n <= 0)
+            n = sm_count_current_device() / 2;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
 static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t s)
 {
-    CUtensorMap tmA, tmB, tmOut, tmR;
+    CUtensorMap tmA, tmB, tmSFA, tmSFB, tmOut, tmR;
     const uint64_t kbytes = (uint64_t)job.K / 2;
+    const int64_t m_tiles = (job.M + BM - 1) / BM;
+    const int64_t n_sf_tiles = (job.N + 127) / 128;
+    const int64_t kb4 = job.K / 64;
+    // Block scales as rows of 256 bytes: one 512-byte tile is two rows.
+    const uint64_t sfa_rows = (uint64_t)(m_tiles * kb4 * 2), sfb_rows = (uint64_t)(n_sf_tiles * kb4 * 2);
     if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, job.a_codes, kbytes, (uint64_t)job.M, kbytes, BK / 2, BM,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, job.w_codes, kbytes, (uint64_t)job.N, kbytes, BK / 2, BN,
-                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, job.w_codes, kbytes, (uint64_t)job.N, kbytes, BK / 2,
+                     BN / 2, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_2d(&tmSFA, CU_TENSOR_MAP_DATA_TYPE_UINT8, job.a_sf, 256, sfa_rows, 256, 256, kSfBox / 256,
+                     CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_map_2d(&tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, job.w_sf, 256, sfb_rows, 256, 256, kSfBox / 256,
+                     CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map_2d(&tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, job.out, (uint64_t)job.N, (uint64_t)job.M,
                      (uint64_t)job.N * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map_2d(&tmR, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, job.resid ? job.resid : job.out, (uint64_t)job.N,
@@ -459,8 +565,6 @@ static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t 
         return cudaErrorInvalidValue;
 
     GemmParams p{};
-    p.a_sf = job.a_sf;
-    p.w_sf = job.w_sf;
     p.a_gscale = job.a_gscale;
     p.w_gscale = job.w_gscale;
     p.bias = static_cast<const __nv_bfloat16*>(job.bias);
@@ -468,11 +572,11 @@ static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t 
     p.M = (int)job.M;
     p.N = (int)job.N;
     p.K = (int)job.K;
-    p.m_tiles = (int)((job.M + BM - 1) / BM);
+    p.m_tiles = (int)m_tiles;
+    p.pair_m_tiles = (int)((m_tiles + 1) / 2);
     p.n_tiles = (int)((job.N + BN - 1) / BN);
     p.k_stages = (int)((job.K + BK - 1) / BK);
-    p.kb4 = (int)(job.K / 64);
-    p.n_sf_tiles = (int)((job.N + 127) / 128);
+    p.kb4 = (int)kb4;
     p.has_resid = job.resid != nullptr ? 1 : 0;
     p.seg = job.seg;
     p.status = job.status;
@@ -487,10 +591,23 @@ static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t 
     });
     if (attr_err != cudaSuccess) return attr_err;
 
-    const int tiles = p.m_tiles * p.n_tiles;
-    const int grid = tiles < sm_count_current_device() ? tiles : sm_count_current_device();
-    nvfp4_gemm_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, tmOut, tmR, p);
-    return cudaGetLastError();
+    const int tiles = p.pair_m_tiles * p.n_tiles;
+    const int max_pairs = max_pairs_current_device();
+    const int pairs = tiles < max_pairs ? tiles : max_pairs;
+    if (pairs <= 0) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (unsigned)pairs);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel, tmA, tmB, tmSFA, tmSFB, tmOut, tmR, p);
 }
 
 }  // namespace h3fp4
