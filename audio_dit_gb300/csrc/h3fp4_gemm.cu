@@ -29,7 +29,7 @@
 //   warp 0      TMA producer (both CTAs): A / W code tiles (128-byte swizzle)
 //               complete on the LEADER's "full" barrier of the stage; this
 //               CTA's block-scale tiles complete on its own "scales landed"
-//               barrier (4-stage ring).
+//               barrier (5-stage ring).
 //   warp 1      TMEM owner (both) + MMA issuer (leader): per stage, once both
 //               CTAs' scales are in TMEM, four paired MMAs, then a commit
 //               multicast to both CTAs' "empty" barrier.
@@ -60,7 +60,7 @@ namespace {
 constexpr int BM = 128;                               // rows of A per CTA (256 per pair)
 constexpr int BN = 256;                               // rows of W per pair tile
 constexpr int BK = 256;                               // K elements per stage
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kThreads = 512;
 constexpr int kScaleWarp0 = 4;   // warps 4..7: scale warps, lane quarter = warp & 3
 constexpr int kEpiWarp0 = 8;     // warps 8..15: epilogue
@@ -75,10 +75,12 @@ constexpr uint32_t kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;  // 
 constexpr uint32_t kPairTxBytes = 2 * (kABytes + kBBytes);  // both CTAs' code tiles complete on the leader
 constexpr uint32_t kSfBox = 2048;                     // scale-tile TMA box: 8 rows x 256 bytes
 constexpr uint32_t kChunkBytes = 32 * 32 * 2;         // 32 rows x 32 bf16
-constexpr uint32_t kEpiWarpBytes = 4 * kChunkBytes;   // 8192
+constexpr uint32_t kEpiWarpBytes = 2 * kChunkBytes;   // 4096: two staging buffers
 constexpr uint32_t kEpiOff = kStages * kStageBytes;
 constexpr uint32_t kBarOff = kEpiOff + kEpiWarps * kEpiWarpBytes;
-constexpr uint32_t kSmemBytes = kBarOff + 256;  // barriers, TMEM address, abort flag
+constexpr uint32_t kBarBytes = 8 * (4 * kStages + 3 + kEpiWarps) + 8;  // barriers, TMEM address, abort flag
+constexpr uint32_t kSmemBytes = kBarOff + 512;
+static_assert(kBarBytes <= 512, "barrier block");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmem = 256;
 constexpr uint32_t kSfTmemPerStage = 48;
@@ -360,11 +362,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (blockIdx.x & 1 is the CTA's rank in its pair)
             const int m0 = (2 * mp + (int)(blockIdx.x & 1u)) * BM + 32 * q;  // first row of this warp
             const int nc0 = nt * BN + 128 * h;                                 // first column of this warp
-            if (lane == 0) bulk_wait_read_all();  // staging buffer free again
+            // Two passes of two 32x32 chunks through the warp's two staging
+            // buffers; the residual chunks of a pass are TMA-loaded into them
+            // first (pass 0 ahead of the accumulator).
+            if (lane == 0) bulk_wait_read_all();  // staging buffers free again
             __syncwarp();
             if (p.has_resid && lane == 0) {
-                mbar_arrive_expect_tx(&rbar[e], 4 * kChunkBytes);
-                for (int c = 0; c < 4; ++c) tma_load_2d(stg + c * kChunkBytes, &tmR, &rbar[e], nc0 + 32 * c, m0);
+                mbar_arrive_expect_tx(&rbar[e], 2 * kChunkBytes);
+                for (int c = 0; c < 2; ++c) tma_load_2d(stg + c * kChunkBytes, &tmR, &rbar[e], nc0 + 32 * c, m0);
             }
             r_pending = p.has_resid != 0;
             bool ok = mbar_wait(acc_full, acc_phase, p.wait_ns, p.status, kStatusTimeoutEpilogue);
@@ -383,73 +388,92 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(acc_empty), 0));  // accumulator free
 
-            if (p.has_resid) {
-                ok = mbar_wait(&rbar[e], r_phase, p.wait_ns, p.status, kStatusTimeoutEpilogue);
-                if (!__all_sync(0xffffffffu, ok)) {
-                    if (lane == 0) set_abort();
-                    break;
-                }
-                r_phase ^= 1u;
-                r_pending = false;
-            }
             const int row = m0 + lane;
             const float* grow = nullptr;
             if (p.gate != nullptr && row < p.M) grow = p.gate + (size_t)segment_of_row(p.seg, row) * p.N;
+            bool failed = false;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint8_t* buf = stg + c * kChunkBytes;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int n8 = nc0 + 32 * c + 8 * j;
-                    float b[8], g[8], r[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        b[i] = 0.0f;
-                        g[i] = 1.0f;
-                        r[i] = 0.0f;
+            for (int pass = 0; pass < 2; ++pass) {
+                if (pass == 1) {
+                    if (lane == 0) bulk_wait_read_all();  // pass 0's stores have read the buffers
+                    __syncwarp();
+                    if (p.has_resid && lane == 0) {
+                        mbar_arrive_expect_tx(&rbar[e], 2 * kChunkBytes);
+                        for (int c = 0; c < 2; ++c)
+                            tma_load_2d(stg + c * kChunkBytes, &tmR, &rbar[e], nc0 + 64 + 32 * c, m0);
                     }
-                    if (n8 < p.N) {
-                        if (p.bias != nullptr) {
-                            const uint4 bv = __ldg(reinterpret_cast<const uint4*>(p.bias + n8));
-                            const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+                    r_pending = p.has_resid != 0;
+                }
+                if (p.has_resid) {
+                    ok = mbar_wait(&rbar[e], r_phase, p.wait_ns, p.status, kStatusTimeoutEpilogue);
+                    if (!__all_sync(0xffffffffu, ok)) {
+                        failed = true;
+                        break;
+                    }
+                    r_phase ^= 1u;
+                    r_pending = false;
+                }
 #pragma unroll
-                            for (int i = 0; i < 4; ++i) {
-                                b[2 * i] = __uint_as_float(bw[i] << 16);
-                                b[2 * i + 1] = __uint_as_float(bw[i] & 0xFFFF0000u);
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = 2 * pass + cc;
+                    uint8_t* buf = stg + cc * kChunkBytes;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int n8 = nc0 + 32 * c + 8 * j;
+                        float b[8], g[8], r[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            b[i] = 0.0f;
+                            g[i] = 1.0f;
+                            r[i] = 0.0f;
+                        }
+                        if (n8 < p.N) {
+                            if (p.bias != nullptr) {
+                                const uint4 bv = __ldg(reinterpret_cast<const uint4*>(p.bias + n8));
+                                const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    b[2 * i] = __uint_as_float(bw[i] << 16);
+                                    b[2 * i + 1] = __uint_as_float(bw[i] & 0xFFFF0000u);
+                                }
+                            }
+                            if (grow != nullptr) {
+                                const float4 g0 = __ldg(reinterpret_cast<const float4*>(grow + n8));
+                                const float4 g1 = __ldg(reinterpret_cast<const float4*>(grow + n8) + 1);
+                                g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
+                                g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
                             }
                         }
-                        if (grow != nullptr) {
-                            const float4 g0 = __ldg(reinterpret_cast<const float4*>(grow + n8));
-                            const float4 g1 = __ldg(reinterpret_cast<const float4*>(grow + n8) + 1);
-                            g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
-                            g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
-                        }
-                    }
-                    uint4* slot = reinterpret_cast<uint4*>(buf + swz64(lane, j));
-                    if (p.has_resid) {
-                        const uint4 rv = *slot;
-                        const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+                        uint4* slot = reinterpret_cast<uint4*>(buf + swz64(lane, j));
+                        if (p.has_resid) {
+                            const uint4 rv = *slot;
+                            const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            r[2 * i] = __uint_as_float(rw[i] << 16);
-                            r[2 * i + 1] = __uint_as_float(rw[i] & 0xFFFF0000u);
+                            for (int i = 0; i < 4; ++i) {
+                                r[2 * i] = __uint_as_float(rw[i] << 16);
+                                r[2 * i + 1] = __uint_as_float(rw[i] & 0xFFFF0000u);
+                            }
                         }
-                    }
-                    float o[8];
+                        float o[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float y = __fmul_rn(__uint_as_float(acc[c][8 * j + i]), alpha);
-                        const float v = __fadd_rn(y, b[i]);
-                        o[i] = (grow != nullptr) ? __fmaf_rn(g[i], v, r[i]) : __fadd_rn(v, r[i]);
+                        for (int i = 0; i < 8; ++i) {
+                            const float y = __fmul_rn(__uint_as_float(acc[c][8 * j + i]), alpha);
+                            const float v = __fadd_rn(y, b[i]);
+                            o[i] = (grow != nullptr) ? __fmaf_rn(g[i], v, r[i]) : __fadd_rn(v, r[i]);
+                        }
+                        *slot = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                                           pack_bf16x2(o[6], o[7]));
                     }
-                    *slot = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
-                                       pack_bf16x2(o[6], o[7]));
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) tma_store_2d(&tmOut, buf, nc0 + 32 * c, m0);
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) tma_store_2d(&tmOut, buf, nc0 + 32 * c, m0);
+                if (lane == 0) bulk_commit();
             }
-            if (lane == 0) bulk_commit();
+            if (failed) {
+                if (lane == 0) set_abort();
+                break;
+            }
         }
         if (r_pending) (void)mbar_wait(&rbar[e], r_phase, p.wait_ns, p.status, kStatusTimeoutEpilogue);
         if (lane == 0) bulk_wait_all();
