@@ -48,6 +48,79 @@ struct QuantParams {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Two fp32 lanes in one 64-bit register for the paired fp32 instructions:
+// fma.rn.f32x2 / mul.rn.f32x2 round each lane exactly like the scalar
+// fma.rn.f32 / mul.rn.f32.
+__device__ __forceinline__ uint64_t f2(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unf2(uint64_t v, float& lo, float& hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Eight fp32 values -> eight E2M1 codes in one word, value 2i in bits 8i..8i+3
+// and value 2i+1 in bits 8i+4..8i+7 (RN, saturating to +-6, sign kept).
+__device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8])
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
+        "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+        : "=r"(r)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    return r;
+}
+
+// E4M3 code (sign clear) -> fp32 through the hardware E4M3 -> f16 conversion
+// (every E4M3 value is exact in f16, and f16 -> f32 is exact).
+__device__ __forceinline__ float e4m3_value(uint32_t code)
+{
+    float f;
+    asm("{\n\t.reg .b16 c, lo, hi;\n\t.reg .b32 h2;\n\t"
+        "cvt.u16.u32 c, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 h2, c;\n\t"
+        "mov.b32 {lo, hi}, h2;\n\t"
+        "cvt.f32.f16 %0, lo;\n\t}"
+        : "=f"(f)
+        : "r"(code));
+    return f;
+}
+
+// RN(b / 6) for b >= 0 a bf16 value (a block maximum), without a division:
+// q = RN(b * RN(1/6)), the remainder b - 6q is exact in one fma, and one more
+// fma applies the correction step of Markstein's FMA-based division.  Equal to
+// the IEEE quotient for every non-negative bf16 value, subnormal quotients
+// included (checked exhaustively).
+__device__ __forceinline__ float div6_bf16(float b)
+{
+    const float c = __uint_as_float(0x3E2AAAABu);  // RN(1/6)
+    const float q = __fmul_rn(b, c);
+    const float r = __fmaf_rn(-q, 6.0f, b);
+    return __fmaf_rn(r, c, q);
+}
+
 // Sixteen bf16 values = 32 bytes: one 256-bit load when the row pointer is
 // 32-byte aligned, two 128-bit loads otherwise.
 struct V16 {
@@ -91,7 +164,7 @@ __device__ __forceinline__ int segment_of(const Segments& s, long long r)
 
 // Per-thread modulation constants for the 16 columns it owns.
 struct ModCols {
-    float onep[16], sh[16];
+    uint64_t onep[8], sh[8];  // (1 + scale, shift) of columns 2j, 2j + 1
     long long seg_end;
 };
 
@@ -103,14 +176,10 @@ __device__ __forceinline__ void load_mod(const QuantParams& p, int seg, int cb, 
     for (int i = 0; i < 4; ++i) {
         const float4 a = __ldg(sc + i);
         const float4 b = __ldg(sh + i);
-        mc.onep[4 * i + 0] = __fadd_rn(1.0f, a.x);
-        mc.onep[4 * i + 1] = __fadd_rn(1.0f, a.y);
-        mc.onep[4 * i + 2] = __fadd_rn(1.0f, a.z);
-        mc.onep[4 * i + 3] = __fadd_rn(1.0f, a.w);
-        mc.sh[4 * i + 0] = b.x;
-        mc.sh[4 * i + 1] = b.y;
-        mc.sh[4 * i + 2] = b.z;
-        mc.sh[4 * i + 3] = b.w;
+        mc.onep[2 * i] = f2(__fadd_rn(1.0f, a.x), __fadd_rn(1.0f, a.y));
+        mc.onep[2 * i + 1] = f2(__fadd_rn(1.0f, a.z), __fadd_rn(1.0f, a.w));
+        mc.sh[2 * i] = f2(b.x, b.y);
+        mc.sh[2 * i + 1] = f2(b.z, b.w);
     }
     mc.seg_end = p.seg.off[seg + 1];
 }
@@ -118,9 +187,9 @@ __device__ __forceinline__ void load_mod(const QuantParams& p, int seg, int cb, 
 __device__ __forceinline__ void init_mod(ModCols& mc)
 {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        mc.onep[j] = 1.0f;
-        mc.sh[j] = 0.0f;
+    for (int j = 0; j < 8; ++j) {
+        mc.onep[j] = f2(1.0f, 1.0f);
+        mc.sh[j] = f2(0.0f, 0.0f);
     }
     mc.seg_end = -1;
 }
@@ -134,8 +203,8 @@ __device__ __forceinline__ void modulate16(float (&f)[16], const ModCols& mc)
     if (kMod) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const float a = __fmaf_rn(f[2 * j], mc.onep[2 * j], mc.sh[2 * j]);
-            const float b = __fmaf_rn(f[2 * j + 1], mc.onep[2 * j + 1], mc.sh[2 * j + 1]);
+            float a, b;
+            unf2(fma2(f2(f[2 * j], f[2 * j + 1]), mc.onep[j], mc.sh[j]), a, b);
             const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
             const uint32_t u = *reinterpret_cast<const uint32_t*>(&h);
             f[2 * j] = bf16_lo(u);
@@ -246,15 +315,15 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(QuantParams p)
             float bmax = 0.0f;
 #pragma unroll
             for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, fabsf(f[j]));
-            const uint32_t S = real ? cvt_e4m3(__fdiv_rn(__fdiv_rn(bmax, 6.0f), s_g)) : 0u;
-            const float eff = __fmul_rn(e4m3_to_f32(S), s_g);
+            const uint32_t S = real ? cvt_e4m3(__fdiv_rn(div6_bf16(bmax), s_g)) : 0u;
+            const float eff = __fmul_rn(e4m3_value(S), s_g);
             const float rcp = (eff == 0.0f) ? 0.0f : fminf(__frcp_rn(eff), FLT_MAX);
-            uint32_t w0 = 0, w1 = 0;
+            const uint64_t rcp2 = f2(rcp, rcp);
+            float q[16];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                w0 |= cvt_e2m1x2(__fmul_rn(f[2 * j], rcp), __fmul_rn(f[2 * j + 1], rcp)) << (8 * j);
-                w1 |= cvt_e2m1x2(__fmul_rn(f[8 + 2 * j], rcp), __fmul_rn(f[9 + 2 * j], rcp)) << (8 * j);
-            }
+            for (int j = 0; j < 8; ++j) unf2(mul2(f2(f[2 * j], f[2 * j + 1]), rcp2), q[2 * j], q[2 * j + 1]);
+            const uint32_t w0 = e2m1x8(reinterpret_cast<const float(&)[8]>(q[0]));
+            const uint32_t w1 = e2m1x8(reinterpret_cast<const float(&)[8]>(q[8]));
             if (valid && real) codes_c[rr * (p.K / 16)] = make_uint2(w0, w1);
             // gather the four block scales of this 64-column group into lane%4 == 0
             const uint32_t s1 = __shfl_down_sync(0xffffffffu, S, 1);
