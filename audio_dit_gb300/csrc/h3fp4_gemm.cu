@@ -188,6 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     cluster_sync();  // both CTAs' barriers and TMEM exist before any cross-CTA traffic
     tc_fence_after();
+    // Everything above overlaps the previous kernel's tail (programmatic
+    // dependent launch); the operands, scales and global scales it may have
+    // produced are read only after this.
+    griddep_wait();
     const uint32_t tmem = *tmem_slot;
     const int num_tiles = p.pair_m_tiles * p.n_tiles;
     // A timeout anywhere stops both CTAs of the pair.
@@ -620,17 +624,19 @@ static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t 
     const int pairs = tiles < max_pairs ? tiles : max_pairs;
     if (pairs <= 0) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(2 * (unsigned)pairs);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = s;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel, tmA, tmB, tmSFA, tmSFB, tmOut, tmR, p);
 }
 

@@ -233,6 +233,8 @@ template <bool kMod, bool kWide>
 __global__ void __launch_bounds__(kThreads) amax_kernel(QuantParams p)
 {
     __shared__ float red[kThreads / 32];
+    griddep_launch_dependents();
+    griddep_wait();  // X and the modulation vectors may come from the previous kernel
     const int cb = blockIdx.x * kThreads + threadIdx.x;  // 16-element block column
     const bool valid = cb < p.K / 16;
     const long long r0 = (long long)blockIdx.y * p.rows_per_cta;
@@ -269,6 +271,8 @@ template <bool kMod, bool kWide>
 __global__ void __launch_bounds__(kThreads) pack_kernel(QuantParams p)
 {
     __shared__ float red[kThreads / 32];
+    griddep_launch_dependents();
+    griddep_wait();  // the amax partials (or the given scale) come from the previous kernel
     // Global scale: one full-activation amax over every partial of pass 1.
     float s_g;
     if (p.gscale_given) {
@@ -394,18 +398,32 @@ QuantParams make_params(const QuantJob& job, dim3* grid)
 // Row starts are 32-byte aligned when the base is (K % 64 == 0).
 bool wide_ok(const void* x) { return (reinterpret_cast<uintptr_t>(x) & 31u) == 0; }
 
-template <bool kMod>
-void launch_amax_t(const QuantParams& p, dim3 grid, bool wide, cudaStream_t s)
+// Both passes launch with programmatic stream serialization: their CTAs may be
+// scheduled while the previous kernel drains and wait for it in-kernel.
+cudaError_t launch_pdl(void (*kernel)(QuantParams), const QuantParams& p, dim3 grid, cudaStream_t s)
 {
-    if (wide) amax_kernel<kMod, true><<<grid, kThreads, 0, s>>>(p);
-    else amax_kernel<kMod, false><<<grid, kThreads, 0, s>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
 template <bool kMod>
-void launch_pack_t(const QuantParams& p, dim3 grid, bool wide, cudaStream_t s)
+cudaError_t launch_amax_t(const QuantParams& p, dim3 grid, bool wide, cudaStream_t s)
 {
-    if (wide) pack_kernel<kMod, true><<<grid, kThreads, 0, s>>>(p);
-    else pack_kernel<kMod, false><<<grid, kThreads, 0, s>>>(p);
+    return launch_pdl(wide ? amax_kernel<kMod, true> : amax_kernel<kMod, false>, p, grid, s);
+}
+
+template <bool kMod>
+cudaError_t launch_pack_t(const QuantParams& p, dim3 grid, bool wide, cudaStream_t s)
+{
+    return launch_pdl(wide ? pack_kernel<kMod, true> : pack_kernel<kMod, false>, p, grid, s);
 }
 
 }  // namespace
@@ -417,23 +435,18 @@ cudaError_t launch_quantize(const QuantJob& job, cudaStream_t s)
     const bool mod = job.shift != nullptr;
     const bool wide = wide_ok(job.x);
     if (!job.gscale_given) {
-        if (mod) launch_amax_t<true>(p, grid, wide, s);
-        else launch_amax_t<false>(p, grid, wide, s);
-        cudaError_t e = cudaGetLastError();
+        const cudaError_t e = mod ? launch_amax_t<true>(p, grid, wide, s) : launch_amax_t<false>(p, grid, wide, s);
         if (e != cudaSuccess) return e;
     }
-    if (mod) launch_pack_t<true>(p, grid, wide, s);
-    else launch_pack_t<false>(p, grid, wide, s);
-    return cudaGetLastError();
+    return mod ? launch_pack_t<true>(p, grid, wide, s) : launch_pack_t<false>(p, grid, wide, s);
 }
 
 cudaError_t launch_amax(const QuantJob& job, float* amax_out, cudaStream_t s)
 {
     dim3 grid;
     const QuantParams p = make_params(job, &grid);
-    if (job.shift != nullptr) launch_amax_t<true>(p, grid, wide_ok(job.x), s);
-    else launch_amax_t<false>(p, grid, wide_ok(job.x), s);
-    cudaError_t e = cudaGetLastError();
+    const cudaError_t e = job.shift != nullptr ? launch_amax_t<true>(p, grid, wide_ok(job.x), s)
+                                               : launch_amax_t<false>(p, grid, wide_ok(job.x), s);
     if (e != cudaSuccess) return e;
     reduce_partials_kernel<<<1, kThreads, 0, s>>>(p.partials, p.nparts, amax_out);
     return cudaGetLastError();

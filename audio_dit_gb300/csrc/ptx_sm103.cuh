@@ -475,4 +475,18 @@ __device__ __forceinline__ void setmaxnreg_inc()
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+//
+// A kernel launched with cudaLaunchAttributeProgrammaticStreamSerialization may
+// start while the previous kernel of the stream drains.  griddep_wait() blocks
+// until that kernel has completed and its memory operations are visible (a
+// no-op when the launch was ordinary); griddep_launch_dependents() lets the
+// next such kernel be scheduled once every CTA of this grid has issued it.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 }  // namespace h3fp4
