@@ -195,28 +195,72 @@ def time_device_steps(torch, A, prob: Problem, steps: int, warmup: int, flush):
     return q, g, wall
 
 
-def time_e2e(torch, A, prob: Problem, steps: int, warmup: int):
-    """Public API end to end: pinned host X (+R) -> device, fused h3fp4_linear, output -> host."""
-    s = torch.cuda.current_stream()
-    x = torch.empty_like(prob.x)
-    resid = None if prob.resid is None else torch.empty_like(prob.resid)
-    out = torch.empty_like(prob.out)
+def time_e2e(torch, A, prob: Problem, steps: int, warmup: int, copy_streams: int = 1):
+    """Public API end to end: each step copies its X (+R) from pinned host memory,
+    runs the fused h3fp4_linear and copies its bf16 output back to pinned host
+    memory. Copies in, compute and copies out run on separate streams with two
+    buffer sets, so one step's output copy overlaps the next step's input copy
+    and compute (a serving pipeline); each copy is split by rows over
+    `copy_streams` streams so that several copy engines share it. Event
+    dependencies keep every buffer from being reused before its previous step
+    is done with it. The timed region spans the first input copy to the last
+    output copy."""
+    main = torch.cuda.current_stream()
+    s_comp = torch.cuda.Stream()
+    ins = [torch.cuda.Stream() for _ in range(copy_streams)]
+    outs_s = [torch.cuda.Stream() for _ in range(copy_streams)]
+    nb = 2
+    xs = [torch.empty_like(prob.x) for _ in range(nb)]
+    rs = [None if prob.resid is None else torch.empty_like(prob.resid) for _ in range(nb)]
+    outs = [torch.empty_like(prob.out) for _ in range(nb)]
+    h_outs = [prob.h_out] + [torch.empty_like(prob.h_out).pin_memory() for _ in range(nb - 1)]
+    ev = lambda: torch.cuda.Event()
+    in_done = [[ev() for _ in range(copy_streams)] for _ in range(nb)]
+    comp_done = [ev() for _ in range(nb)]
+    out_done = [[ev() for _ in range(copy_streams)] for _ in range(nb)]
+    used = [False] * nb
+    rows = lambda t, c: t.narrow(0, c * t.shape[0] // copy_streams,
+                                 (c + 1) * t.shape[0] // copy_streams - c * t.shape[0] // copy_streams)
 
-    def step():
-        x.copy_(prob.h_x, non_blocking=True)
-        if resid is not None:
-            resid.copy_(prob.h_resid, non_blocking=True)
-        prob.fused_from_device(A, x, resid, out)
-        prob.h_out.copy_(out, non_blocking=True)
+    def step(i):
+        b = i % nb
+        for c, st in enumerate(ins):
+            with torch.cuda.stream(st):
+                if used[b]:
+                    st.wait_event(comp_done[b])          # step i-2 has consumed xs[b] / rs[b]
+                rows(xs[b], c).copy_(rows(prob.h_x, c), non_blocking=True)
+                if rs[b] is not None:
+                    rows(rs[b], c).copy_(rows(prob.h_resid, c), non_blocking=True)
+                in_done[b][c].record(st)
+        with torch.cuda.stream(s_comp):
+            for c in range(copy_streams):
+                s_comp.wait_event(in_done[b][c])
+                if used[b]:
+                    s_comp.wait_event(out_done[b][c])    # step i-2's output copy has read outs[b]
+            prob.fused_from_device(A, xs[b], rs[b], outs[b])
+            comp_done[b].record(s_comp)
+        for c, st in enumerate(outs_s):
+            with torch.cuda.stream(st):
+                st.wait_event(comp_done[b])
+                rows(h_outs[b], c).copy_(rows(outs[b], c), non_blocking=True)
+                out_done[b][c].record(st)
+        used[b] = True
 
-    for _ in range(warmup):
-        step()
+    streams = [s_comp] + ins + outs_s
+    for st in streams:
+        st.wait_stream(main)
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s)
-    for _ in range(steps):
-        step()
-    e1.record(s)
+    e0.record(main)
+    for st in streams:
+        st.wait_event(e0)
+    for i in range(steps):
+        step(warmup + i)
+    for st in streams:
+        main.wait_stream(st)
+    e1.record(main)
     torch.cuda.synchronize()
     A.h3fp4_check(prob.ws)
     ms = e0.elapsed_time(e1) / steps
