@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kThreads) pack_kernel(QuantParams p)
         for (int u = 0; u < kRowUnroll; ++u) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) v[u].w[i] = 0u;
-            if (valid && r + u < p.rows) v[u] = ld16<kWide>(xc + (r + u) * p.K);
+            if (valid && r + u < r1 && r + u < p.rows) v[u] = ld16<kWide>(xc + (r + u) * p.K);
         }
 #pragma unroll
         for (int u = 0; u < kRowUnroll; ++u) {
@@ -387,8 +387,14 @@ QuantParams make_params(const QuantJob& job, dim3* grid)
     int row_groups = (target + col_ctas - 1) / col_ctas;
     row_groups = max(1, min(row_groups, kMaxPartials / col_ctas));
     // rows per CTA covers the padded rows so the pack pass zeroes scale padding
+    // Rows per CTA are a multiple of the unroll depth unless that rounding would
+    // leave more than 5 % of the wave's CTA slots empty (small activations).
     p.rows_per_cta = (int)((p.rows_pad + row_groups - 1) / row_groups);
-    p.rows_per_cta = (p.rows_per_cta + kRowUnroll - 1) / kRowUnroll * kRowUnroll;
+    {
+        const int rounded = (p.rows_per_cta + kRowUnroll - 1) / kRowUnroll * kRowUnroll;
+        const long long groups = (p.rows_pad + rounded - 1) / rounded;
+        if (groups * col_ctas * 100 >= (long long)target * 95) p.rows_per_cta = rounded;
+    }
     row_groups = (int)((p.rows_pad + p.rows_per_cta - 1) / p.rows_per_cta);
     p.nparts = col_ctas * row_groups;
     *grid = dim3(col_ctas, row_groups);
