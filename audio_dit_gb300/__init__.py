@@ -20,7 +20,7 @@ __all__ = [
     "H3FP4Error", "PROLOGUE_MOD", "EPI_BIAS", "EPI_GATE_RESID", "GSCALE_GIVEN", "A_PREQUANT",
     "MAX_SEGMENTS", "library_path", "load_library", "h3fp4_codes_bytes", "h3fp4_sf_bytes",
     "h3fp4_workspace_bytes", "h3fp4_quantize_weight", "h3fp4_quantize_act", "h3fp4_linear",
-    "h3fp4_check", "h3fp4_act_amax", "h3fp4_gscale_from_amax", "h3fp4_selftest_timeout", "h3fp4_measure_fp4_peak", "h3fp4_quantize_act_noalloc",
+    "h3fp4_check", "h3fp4_act_amax", "h3fp4_gscale_from_amax", "h3fp4_selftest_timeout", "h3fp4_measure_fp4_peak", "h3fp4_measure_fp4_pair_peak", "h3fp4_quantize_act_noalloc",
     "h3fp4_set_wait_limit_ns", "h3fp4_status_string", "alloc_nvfp4", "alloc_workspace",
 ]
 
@@ -67,6 +67,7 @@ def load_library():
         "h3fp4_gscale_from_amax": (i32, [vp, vp, vp]),
         "h3fp4_selftest_timeout": (i32, [vp, C.c_uint64, vp]),
         "h3fp4_measure_fp4_peak": (i32, [i32, vp, vp]),
+        "h3fp4_measure_fp4_pair_peak": (i32, [i32, vp, vp]),
         "h3fp4_quantize_act_noalloc": (i32, [vp, i64, i64, vp, vp, vp, i32, vp, vp, vp, i32, vp]),
         "h3fp4_check": (i32, [vp, vp]),
         "h3fp4_set_wait_limit_ns": (None, [C.c_uint64]),
@@ -235,6 +236,14 @@ def h3fp4_measure_fp4_peak(ws: torch.Tensor, iters: int = 20000) -> float:
     out = C.c_float(0.0)
     _check(load_library().h3fp4_measure_fp4_peak(int(iters), C.byref(out), _ptr(ws, "ws", torch.uint8)),
            "h3fp4_measure_fp4_peak")
+    return float(out.value)
+
+
+def h3fp4_measure_fp4_pair_peak(ws: torch.Tensor, iters: int = 20000) -> float:
+    """Measured ceiling (TFLOP/s) of the paired (2-CTA) FP4 MMA the GEMM issues (synchronous)."""
+    out = C.c_float(0.0)
+    _check(load_library().h3fp4_measure_fp4_pair_peak(int(iters), C.byref(out), _ptr(ws, "ws", torch.uint8)),
+           "h3fp4_measure_fp4_pair_peak")
     return float(out.value)
 
 

@@ -75,4 +75,7 @@ int sm_count_current_device();
 // Synchronous: FP4 MMA loop on every SM, returns TFLOP/s (status word for its bounded wait).
 cudaError_t measure_fp4_peak(int iters, unsigned int* status, float* tflops);
 
+// The same for the paired (cta_group::2) MMA on every 2-CTA cluster.
+cudaError_t measure_fp4_pair_peak(int iters, unsigned int* status, float* tflops);
+
 }  // namespace h3fp4

@@ -338,6 +338,7 @@ def run_gpu(args):
     value = world * prob.flops / (step_ms * 1e-3) / 1e12
     fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
     mma_peak = A.h3fp4_measure_fp4_peak(prob.ws, 20000) if rank == 0 else None
+    pair_peak = A.h3fp4_measure_fp4_pair_peak(prob.ws, 20000) if rank == 0 else None
     gemm_ms = float(np.mean(g))
     gemm_tflops = prob.flops / (gemm_ms * 1e-3) / 1e12
     qb = prob.quant_bytes()
@@ -398,6 +399,8 @@ def run_gpu(args):
                          "peak_source": f"{peaks['source']} bf16 burst {peaks['bf16_tflops']} x nominal fp4/bf16 6",
                          "measured_mma_peak": round(mma_peak, 1) if mma_peak else None,
                          "frac_of_measured_mma_peak": round(gemm_tflops / mma_peak, 4) if mma_peak else None,
+                         "measured_pair_mma_peak": round(pair_peak, 1) if pair_peak else None,
+                         "frac_of_measured_pair_mma_peak": round(gemm_tflops / pair_peak, 4) if pair_peak else None,
                          "traffic": NCU_GEMM_TRAFFIC.get(args.config), "algorithmic_bytes": prob.gemm_bytes()},
             "quant": {"gbs": round(quant_gbs, 1), "peak_gbs": peaks["hbm_gbs"],
                       "frac": round(quant_gbs / peaks["hbm_gbs"], 4), "ms": round(quant_ms, 5),

@@ -203,6 +203,13 @@ H3FP4_API h3fp4_status h3fp4_selftest_timeout(void* ws, uint64_t limit_ns, cudaS
  * nominal dense FP4 figure. */
 H3FP4_API h3fp4_status h3fp4_measure_fp4_peak(int iters, float* tflops, void* ws);
 
+/* The same ceiling for the paired form the GEMM issues:
+ * tcgen05.mma.cta_group::2 (M=256 over a 2-CTA cluster, N=256, K=64), `iters`
+ * MMAs by the leader of every cluster that fits on the device (synchronous,
+ * default stream).  Writes TFLOP/s to *tflops; ws: any workspace (status word
+ * only).  No counterpart in the pages: it measures this GPU. */
+H3FP4_API h3fp4_status h3fp4_measure_fp4_pair_peak(int iters, float* tflops, void* ws);
+
 /* Synchronises `stream`, reads and clears the workspace status word.
  * Returns H3FP4_OK, or H3FP4_ERR_TIMEOUT when a kernel gave up early (a
  * bounded device wait ran out, or shared memory came up misaligned); the
