@@ -268,7 +268,7 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(QuantParams p)
 // ------------------------------------------------------------------ pass 2: pack
 
 template <bool kMod, bool kWide>
-__global__ void __launch_bounds__(kThreads) pack_kernel(QuantParams p)
+__global__ void __launch_bounds__(kThreads, 10) pack_kernel(QuantParams p)
 {
     __shared__ float red[kThreads / 32];
     griddep_launch_dependents();
