@@ -150,6 +150,11 @@ class Problem:
     def quant(self, A):
         A.h3fp4_quantize_act(self.x, *self.aq, self.ws, shift=self.shift, scale=self.scale, seg_off=self.seg_off)
 
+    def quant_given(self, A):
+        """Pack pass only: the global scale is the one the last in-run quantisation left."""
+        A.h3fp4_quantize_act(self.x, *self.aq, self.ws, shift=self.shift, scale=self.scale, seg_off=self.seg_off,
+                             gscale_given=True)
+
     def gemm(self, A):
         A.h3fp4_linear(self.aq[0], *self.wq, self.out, self.ws, a_sf=self.aq[1], a_gscale=self.aq[2],
                        gate=self.gate, resid=self.resid, bias=self.bias, seg_off=self.seg_off)
@@ -170,12 +175,17 @@ class Problem:
         return b
 
 
-def time_device_steps(torch, A, prob: Problem, steps: int, warmup: int, flush):
-    """Per-step CUDA events on the launching stream: [quant | gemm], L2 flushed between steps."""
+def time_device_steps(torch, A, prob: Problem, steps: int, warmup: int, flush, given_scale: bool = False):
+    """Per-step CUDA events on the launching stream: [quant | gemm], L2 flushed
+    between steps. With given_scale the quantisation is the pack pass alone
+    (the caller supplies the global scale, as a serving loop with calibrated
+    scales would)."""
     s = torch.cuda.current_stream()
+    quant = prob.quant_given if given_scale else prob.quant
+    prob.quant(A)  # leaves a global scale behind for the given-scale variant
     for _ in range(warmup):
         flush()
-        prob.quant(A)
+        quant(A)
         prob.gemm(A)
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
@@ -183,7 +193,7 @@ def time_device_steps(torch, A, prob: Problem, steps: int, warmup: int, flush):
     for i in range(steps):
         flush()
         ev[i][0].record(s)
-        prob.quant(A)
+        quant(A)
         ev[i][1].record(s)
         prob.gemm(A)
         ev[i][2].record(s)
@@ -345,12 +355,22 @@ def run_gpu(args):
     quant_ms = float(np.mean(q))
     quant_gbs = (qb["amax"] + qb["pack"]) / (quant_ms * 1e-3) / 1e9
 
+    given = None
+    if rank == 0:
+        qg, gg, _ = time_device_steps(torch, A, prob, max(5, min(500, args.steps // 4)), 3, flush, given_scale=True)
+        given = {"tflops": round(prob.flops / (np.mean(qg + gg) * 1e-3) / 1e12, 1),
+                 "quant_ms": round(float(np.mean(qg)), 5),
+                 "quant_gbs": round(qb["pack"] / (np.mean(qg) * 1e-3) / 1e9, 1),
+                 "note": "global scale supplied by the caller: pack pass + GEMM"}
+
     extra = {}
     if rank == 0 and not args.no_extra:
-        for name in [c for c in ["fc1", "fc2", "attn_out"] if c != args.config]:
+        for name in [c for c in ["tiny", "fc1", "fc2", "attn_out"] if c != args.config]:
             try:
                 pe = Problem(name, torch, A)
                 qe, ge, _ = time_device_steps(torch, A, pe, max(5, min(200, args.steps // 4)), 3, flush)
+                qge, gge, _ = time_device_steps(torch, A, pe, max(5, min(200, args.steps // 4)), 3, flush,
+                                                given_scale=True)
                 qbe = pe.quant_bytes()
                 extra[name] = {
                     "tflops": round(pe.flops / (np.mean(qe + ge) * 1e-3) / 1e12, 1),
@@ -358,6 +378,8 @@ def run_gpu(args):
                     "gemm_frac_fp4_peak": round(pe.flops / (np.mean(ge) * 1e-3) / 1e12 / fp4_peak, 4),
                     "quant_gbs": round((qbe["amax"] + qbe["pack"]) / (np.mean(qe) * 1e-3) / 1e9, 1),
                     "ms_per_step": round(float(np.mean(qe + ge)), 4),
+                    "given_scale_tflops": round(pe.flops / (np.mean(qge + gge) * 1e-3) / 1e12, 1),
+                    "given_scale_quant_gbs": round(qbe["pack"] / (np.mean(qge) * 1e-3) / 1e9, 1),
                 }
                 del pe
                 torch.cuda.empty_cache()
@@ -409,6 +431,8 @@ def run_gpu(args):
             "clocks": clk.summary(),
             "wall_s_timed": round(wall, 3),
         }
+        if given:
+            line["given_scale"] = given
         if extra:
             line["also"] = extra
         if cpu:
