@@ -34,6 +34,7 @@ FP4_OVER_BF16 = 6.0   # nominal dense fp4 / bf16 tensor ratio (13.5 / 2.25 PFLOP
 DEFAULT_CONFIG = "qkv"
 # DRAM bytes (read + write) per launch of nvfp4_gemm_kernel from one ncu capture
 # of the current kernel (profiles/nvfp4_gemm_qkv.md); None where not captured.
+REFERENCE_BUDGET_S = 120.0  # CPU seconds the reference arm's timed steps aim for in total
 NCU_GEMM_TRAFFIC = {"qkv": 30.30144e6 + 99.238656e6}
 
 
@@ -279,20 +280,36 @@ def time_e2e(torch, A, prob: Problem, steps: int, warmup: int, copy_streams: int
     return ms, h2d, d2h
 
 
+class OracleSample:
+    """The CPU oracle, as it stands, on the first rows of a workload: quantise
+    those rows of X (their own amax), then every output of those rows in
+    float64 (GEMM + epilogue). W is quantised once beforehand (offline, as the
+    method quantises weights); it is not part of a step."""
+
+    def __init__(self, name: str, rows: int):
+        import oracle
+        import workloads as W
+        self.oracle = oracle
+        self.d = W.make_inputs(name, M=rows)
+        self.w = oracle.quantize(self.d["w"])
+
+    def step(self, rows: int):
+        """Returns (TFLOP/s, seconds) for the first `rows` rows."""
+        d = self.d
+        seg = np.minimum(d["seg_off"], rows)
+        t0 = time.perf_counter()
+        a = self.oracle.quantize(d["x"][:rows], d["shift"], d["scale"], seg)
+        self.oracle.linear_full(a, self.w, rows, d["N"], d["K"], bias=d["bias"], gate=d["gate"],
+                                resid=None if d["resid"] is None else d["resid"][:rows], seg_off=seg)
+        dt = time.perf_counter() - t0
+        return 2.0 * rows * d["N"] * d["K"] / dt / 1e12, dt
+
+
 def oracle_sample(name: str, rows: int):
-    """The CPU oracle, as it stands, on the first `rows` rows of the workload:
-    quantise X (its own amax) and W, then every output of those rows in float64."""
-    import oracle
-    import workloads as W
-    d = W.make_inputs(name, M=rows)
-    t0 = time.perf_counter()
-    a = oracle.quantize(d["x"], d["shift"], d["scale"], d["seg_off"])
-    w = oracle.quantize(d["w"])
-    oracle.linear_full(a, w, rows, d["N"], d["K"], bias=d["bias"], gate=d["gate"], resid=d["resid"],
-                       seg_off=d["seg_off"])
-    dt = time.perf_counter() - t0
-    flops = 2.0 * rows * d["N"] * d["K"]
-    return flops / dt / 1e12, dt, oracle.num_threads()
+    """One timed oracle step on the first `rows` rows (see OracleSample)."""
+    s = OracleSample(name, rows)
+    tf, dt = s.step(rows)
+    return tf, dt, s.oracle.num_threads()
 
 
 def run_gpu(args):
@@ -391,8 +408,8 @@ def run_gpu(args):
         rows = args.cpu_rows
         tf, dt, cores = oracle_sample(args.config, rows)
         cpu = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
-               "sample": f"first {rows} rows of {args.config} (own amax), W quantised, all {rows}x{prob.N} "
-                         f"outputs in float64; {dt:.1f} s"}
+               "sample": f"first {rows} rows of {args.config} (own amax), all {rows}x{prob.N} outputs in "
+                         f"float64, W quantised once beforehand; {dt:.1f} s"}
 
     if rank == 0:
         line = {
@@ -446,6 +463,10 @@ def run_gpu(args):
 # ---------------------------------------------------------------------------- reference arm (oracle)
 
 def run_reference(args):
+    """The oracle as the reference arm, timed on the host cores. Each step is a
+    bounded sample of the workload: its rows per step are chosen from the
+    warm-up's time per row so that all --steps steps take about
+    REFERENCE_BUDGET_S seconds (at most 256 rows per step)."""
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
@@ -453,16 +474,21 @@ def run_reference(args):
     import workloads as W
     import oracle
     oracle.build()
-    rows = args.cpu_rows
+    max_rows = args.cpu_rows
+    sample = OracleSample(args.config, max_rows)
+    per_row = []
     for _ in range(args.warmup):
-        oracle_sample(args.config, max(8, rows // 8))
+        _, dt = sample.step(8)
+        per_row.append(dt / 8)
+    per_row_s = float(np.median(per_row)) if per_row else 0.03
+    rows = int(max(1, min(max_rows, REFERENCE_BUDGET_S / max(1, args.steps) / max(per_row_s, 1e-6))))
     vals, times = [], []
     for _ in range(args.steps):
-        tf, dt, cores = oracle_sample(args.config, rows)
+        tf, dt = sample.step(rows)
         vals.append(tf)
         times.append(dt)
     wl = W.WORKLOADS[args.config]
-    v = float(np.mean(vals))
+    v = float(2.0 * rows * wl.N * wl.K * len(times) / sum(times) / 1e12)
     line = {
         "impl": "reference",
         "metric": METRIC,
@@ -477,10 +503,11 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64 (oracle: fp32 quantiser, float64 GEMM)",
         "data": "synthetic (seeded, shapes/distributions of the workload set)",
-        "config": {"workload": f"{wl.name}: first {rows} rows of X [{wl.M},{wl.K}], W [{wl.N},{wl.K}]",
+        "config": {"workload": f"{wl.name}: first {rows} rows of X [{wl.M},{wl.K}] per step, W [{wl.N},{wl.K}]",
                    "M": rows, "N": wl.N, "K": wl.K},
         "cpu_baseline": {"value": v, "unit": "TFLOPS", "cores": oracle.num_threads(), "kind": "oracle",
-                         "sample": f"{rows} rows of {wl.name} per step"},
+                         "sample": f"{rows} rows of {wl.name} per step (quantise + float64 GEMM/epilogue; "
+                                   f"W quantised once beforehand)"},
         "e2e": {"value": v, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
