@@ -14,8 +14,7 @@
 // SM's tensor core multiplies its own 128 rows of A by all 256 rows of W,
 // fetching the other half of W from its partner.  Compared with one CTA per
 // 128 x 256 tile this cuts the bytes each SM pulls from L2 per MMA by 30 %
-// (A 4 KB + W 4 KB + scales 1.5 KB instead of 4 + 8 + 1.5 KB) and halves the
-// number of block-scale copies per flop (one paired copy fills both SMs).
+// (A 4 KB + W 4 KB + scales 1.5 KB instead of 4 + 8 + 1.5 KB).
 //
 // Block scales reach TMEM through registers.  The MMA reads the scales of
 // every row of W from all four TMEM lane quarters, so each quarter holds its
@@ -38,11 +37,15 @@
 //               columns, then an arrival on the leader's "scales ready".
 //   warps 8-15  epilogue (both): tcgen05.ld the CTA's 128 x 256 fp32
 //               accumulator (each warp 32 rows x 128 columns), release it to
-//               the leader, then alpha/bias/gate/residual in fp32, bf16 into a
-//               64-byte-swizzled staging tile and TMA store; the residual tile
-//               is TMA-loaded into the same staging buffer ahead of time.
+//               the leader, then alpha/bias/gate/residual in fp32 and bf16
+//               stores in two passes of two 32x32 chunks, each through two
+//               64-byte-swizzled staging buffers and TMA stores; a pass's
+//               residual chunks are TMA-loaded into those buffers first.
+// Each kernel launch may start while the previous kernel of the stream drains
+// (programmatic dependent launch); it reads no input before griddepcontrol.wait.
 // Registers per thread (setmaxnreg): warpgroup 0: 40, scale warps: 96,
-// epilogue: 184 (40 + 96 + 2 x 184 = 504 <= 512 x 128 / 128 launched).
+// epilogue: 184.  Per 128-thread warpgroup that is 40 + 96 + 2 x 184 = 504
+// registers per thread-slot, within the 4 x 128 the CTA is launched with.
 //
 #include <cstdint>
 #include <cstdio>
