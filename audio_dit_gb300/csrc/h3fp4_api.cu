@@ -69,6 +69,26 @@ h3fp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? H3FP4_OK : H3F
 
 }  // namespace
 
+cudaError_t ensure_dynamic_smem(const void* func, int bytes)
+{
+    struct Entry {
+        const void* func;
+        int dev;
+    };
+    static std::mutex mu;
+    static Entry done[4 * kMaxDevices];
+    static int ndone = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < ndone; ++i)
+        if (done[i].func == func && done[i].dev == dev) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && ndone < 4 * kMaxDevices) done[ndone++] = Entry{func, dev};
+    return e;
+}
+
 int sm_count_current_device()
 {
     int dev = 0;

@@ -614,12 +614,7 @@ static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t 
     p.wait_ns = job.wait_limit_ns;
     p.stall = stall;
 
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(nvfp4_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kSmemBytes);
-    });
+    const cudaError_t attr_err = ensure_dynamic_smem(reinterpret_cast<const void*>(nvfp4_gemm_kernel), (int)kSmemBytes);
     if (attr_err != cudaSuccess) return attr_err;
 
     const int tiles = p.pair_m_tiles * p.n_tiles;

@@ -72,6 +72,11 @@ cudaError_t launch_gscale_from_amax(const float* amax, float* gscale, cudaStream
 
 int sm_count_current_device();
 
+// Sets cudaFuncAttributeMaxDynamicSharedMemorySize of `func` on the current
+// device the first time it is asked for that (function, device) pair; the
+// attribute belongs to each device's context.
+cudaError_t ensure_dynamic_smem(const void* func, int bytes);
+
 // Synchronous: FP4 MMA loop on every SM, returns TFLOP/s (status word for its bounded wait).
 cudaError_t measure_fp4_peak(int iters, unsigned int* status, float* tflops);
 

@@ -124,12 +124,9 @@ __global__ void __launch_bounds__(128, 1) mma_pair_peak_kernel(int iters, unsign
 
 cudaError_t measure_fp4_pair_peak(int iters, unsigned int* status, float* tflops)
 {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e =
-            cudaFuncSetAttribute(mma_pair_peak_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem);
+    {
+        const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(mma_pair_peak_kernel), kPairSmem);
         if (e != cudaSuccess) return e;
-        attr = true;
     }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute at[1];
@@ -170,11 +167,9 @@ cudaError_t measure_fp4_pair_peak(int iters, unsigned int* status, float* tflops
 
 cudaError_t measure_fp4_peak(int iters, unsigned int* status, float* tflops)
 {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(mma_peak_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPeakSmem);
+    {
+        const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(mma_peak_kernel), kPeakSmem);
         if (e != cudaSuccess) return e;
-        attr = true;
     }
     const int sms = sm_count_current_device();
     cudaEvent_t e0, e1;

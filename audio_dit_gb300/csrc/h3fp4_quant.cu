@@ -376,13 +376,13 @@ QuantParams make_params(const QuantJob& job, dim3* grid)
     const int col_ctas = (int)((job.K / 16 + kThreads - 1) / kThreads);
     // One full wave of resident CTAs (the slowest variant's occupancy), each
     // walking a contiguous range of rows: no half-empty second wave.
-    static int per_sm = 0;
-    if (per_sm == 0) {
+    // (thread-safe one-time initialisation; every accepted device is sm_103)
+    static const int per_sm = [] {
         int a = 0, b = 0;
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, pack_kernel<true, true>, kThreads, 0);
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, amax_kernel<true, true>, kThreads, 0);
-        per_sm = max(1, min(a, b));
-    }
+        return max(1, min(a, b));
+    }();
     const int target = sm_count_current_device() * per_sm;
     int row_groups = (target + col_ctas - 1) / col_ctas;
     row_groups = max(1, min(row_groups, kMaxPartials / col_ctas));
