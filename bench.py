@@ -291,25 +291,34 @@ class OracleSample:
         import workloads as W
         self.oracle = oracle
         self.d = W.make_inputs(name, M=rows)
+        t0 = time.perf_counter()
         self.w = oracle.quantize(self.d["w"])
+        self.quantize_w_s = time.perf_counter() - t0
+        self.last_split = (0.0, 0.0)
 
     def step(self, rows: int):
-        """Returns (TFLOP/s, seconds) for the first `rows` rows."""
+        """Returns (TFLOP/s, seconds) for the first `rows` rows; the split
+        (quantise X, GEMM + epilogue) in seconds is kept in last_split."""
         d = self.d
         seg = np.minimum(d["seg_off"], rows)
         t0 = time.perf_counter()
         a = self.oracle.quantize(d["x"][:rows], d["shift"], d["scale"], seg)
+        t1 = time.perf_counter()
         self.oracle.linear_full(a, self.w, rows, d["N"], d["K"], bias=d["bias"], gate=d["gate"],
                                 resid=None if d["resid"] is None else d["resid"][:rows], seg_off=seg)
-        dt = time.perf_counter() - t0
-        return 2.0 * rows * d["N"] * d["K"] / dt / 1e12, dt
+        t2 = time.perf_counter()
+        self.last_split = (t1 - t0, t2 - t1)
+        return 2.0 * rows * d["N"] * d["K"] / (t2 - t0) / 1e12, t2 - t0
 
 
 def oracle_sample(name: str, rows: int):
-    """One timed oracle step on the first `rows` rows (see OracleSample)."""
+    """One timed oracle step on the first `rows` rows (see OracleSample).
+    Returns (TFLOP/s, seconds, threads, {quantise_x_s, gemm_epilogue_s, quantise_w_s})."""
     s = OracleSample(name, rows)
     tf, dt = s.step(rows)
-    return tf, dt, s.oracle.num_threads()
+    split = {"quantise_x_s": round(s.last_split[0], 3), "gemm_epilogue_s": round(s.last_split[1], 3),
+             "quantise_w_s": round(s.quantize_w_s, 3)}
+    return tf, dt, s.oracle.num_threads(), split
 
 
 def run_gpu(args):
@@ -406,8 +415,8 @@ def run_gpu(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rows = args.cpu_rows
-        tf, dt, cores = oracle_sample(args.config, rows)
-        cpu = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+        tf, dt, cores, split = oracle_sample(args.config, rows)
+        cpu = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "split": split,
                "sample": f"first {rows} rows of {args.config} (own amax), all {rows}x{prob.N} outputs in "
                          f"float64, W quantised once beforehand; {dt:.1f} s"}
 
@@ -445,6 +454,11 @@ def run_gpu(args):
                       "frac": round(quant_gbs / peaks["hbm_gbs"], 4), "ms": round(quant_ms, 5),
                       "bytes": "amax read 2 B/elem + pack read 2 + codes 0.5 + scales 1/16 B/elem"},
             "gemm_ms": round(gemm_ms, 5),
+            "timing": {"gemm_ms_median": round(float(np.median(g)), 5), "gemm_ms_best": round(float(np.min(g)), 5),
+                       "quant_ms_median": round(float(np.median(q)), 5), "quant_ms_best": round(float(np.min(q)), 5),
+                       "step_ms_median": round(float(np.median(q + g)), 5),
+                       "step_ms_best": round(float(np.min(q + g)), 5),
+                       "note": "value, gemm_ms and quant.ms are means over the timed steps"},
             "clocks": clk.summary(),
             "wall_s_timed": round(wall, 3),
         }
