@@ -53,6 +53,13 @@
  *     H3FP4_ERR_SHAPE / H3FP4_ERR_ALIGN and launch nothing.
  *   - Only sm_103 devices are accepted (H3FP4_ERR_UNSUPPORTED_DEVICE
  *     otherwise).  There is no CPU fallback and no other backend.
+ *   - Kernels launch with programmatic dependent launch: a kernel may start
+ *     its prologue while the previous kernel of the stream drains, and reads
+ *     nothing written before it until that kernel has completed.  Stream
+ *     order is unchanged.
+ *   - The GEMM runs as clusters of two CTAs (512 threads, ~228 KB of shared
+ *     memory and all 512 TMEM columns each), one CTA per SM, over every SM
+ *     pair that can be co-resident.
  */
 #ifndef H3FP4_H
 #define H3FP4_H
