@@ -29,12 +29,16 @@
 //               complete on the LEADER's "full" barrier of the stage; this
 //               CTA's block-scale tiles complete on its own "scales landed"
 //               barrier (5-stage ring).
-//   warp 1      TMEM owner (both) + MMA issuer (leader): per stage, once both
-//               CTAs' scales are in TMEM, four paired MMAs, then a commit
+//   warp 1      TMEM owner (both) + MMA issuer (leader): per stage, one wait
+//               on the leader's "scales ready", four paired MMAs, then a commit
 //               multicast to both CTAs' "empty" barrier.
 //   warps 4-7   scale warps (both), warp 4 + q serving lane quarter q: per
 //               stage twelve 16-byte shared loads per lane, tcgen05.st of 48
-//               columns, then an arrival on the leader's "scales ready".
+//               columns, then an arrival on the leader's "scales ready".  The
+//               leader's scale warps arrive only after the stage's code tiles
+//               of both CTAs landed too, so "scales ready" alone clears a stage
+//               for the MMAs: every wait in the issuing thread stalls the
+//               tensor pipe (about 75 cycles per extra wait per 513-cycle stage).
 //   warps 8-15  epilogue (both): tcgen05.ld the CTA's 128 x 256 fp32
 //               accumulator (each warp 32 rows x 128 columns), release it to
 //               the leader, then alpha/bias/gate/residual in fp32 and bf16
@@ -155,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);  // leader's: both CTAs' code tiles
     uint64_t* empty = full + kStages;                                // both: the MMAs released the stage
     uint64_t* sf_full = empty + kStages;                             // both: this CTA's scale tiles landed
-    uint64_t* sfready = sf_full + kStages;                           // leader's: both CTAs' scales in TMEM
+    uint64_t* sfready = sf_full + kStages;  // leader's: both CTAs' scales in TMEM and code tiles landed
     uint64_t* acc_full = sfready + kStages;                          // both: accumulator complete
     uint64_t* acc_empty = acc_full + 1;                              // leader's: both epilogues drained
     uint64_t* rbar = acc_empty + 1;                                  // one per epilogue warp
@@ -259,8 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 bool ok = true;
                 for (int kb = 0; kb < p.k_stages; ++kb) {
-                    if (!mbar_wait(&sfready[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma) ||
-                        !mbar_wait(&full[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma)) {
+                    if (!mbar_wait(&sfready[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma)) {
                         ok = false;
                         break;
                     }
@@ -313,6 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 ok = mbar_wait(&sf_full[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma);
+                // The leader's arrival also vouches for both CTAs' code tiles.
+                if (ok && leader) ok = mbar_wait(&full[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
