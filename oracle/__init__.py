@@ -79,6 +79,8 @@ def lib():
                 "orc_linear_full": (None, [C.POINTER(LinearArgs), vp, vp]),
                 "orc_gemm_f64": (None, [vp, vp, i64, i64, i64, vp]),
                 "orc_num_threads": (C.c_int, []),
+                "orc_swiglu_bf16": (C.c_uint16, [C.c_uint16, C.c_uint16]),
+                "orc_swiglu_rows": (None, [vp, i64, i64, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -245,6 +247,22 @@ def linear_points(a, w, M, N, K, points, bias=None, gate=None, resid=None, seg_o
     bound = np.empty(len(pts), np.float64)
     lib().orc_linear_points(C.byref(args), _p(pts), len(pts), _p(out), _p(bound))
     return out, bound
+
+
+def swiglu_bf16(g: int, u: int) -> int:
+    """bf16(silu(g) * u) for bf16 bit patterns g, u (gate and up FC1 outputs)."""
+    return int(lib().orc_swiglu_bf16(g, u))
+
+
+def swiglu_rows(y_bf16) -> np.ndarray:
+    """SwiGLU over an FC1 output in the 256-column [gate 128 | up 128] group
+    layout: y uint16 [rows, 2H] -> h uint16 [rows, H]."""
+    y = _c(y_bf16, np.uint16)
+    rows, n2 = y.shape
+    assert n2 % 256 == 0
+    h = np.empty((rows, n2 // 2), np.uint16)
+    lib().orc_swiglu_rows(_p(y), rows, n2 // 2, _p(h))
+    return h
 
 
 def gemm_f64(a: np.ndarray, w: np.ndarray) -> np.ndarray:

@@ -42,6 +42,10 @@
  *      ((r/128)*Kb4 + c/4)*512 + (r%32)*16 + ((r%128)/32)*4 + c%4,
  *      Kb4 = ceil(K/64); padding bytes are zero.
  *   R7 segments: rows [seg_off[i], seg_off[i+1]) use shift/scale/gate row i.
+ *   R8 SwiGLU producer ([CS], the exact SwiGLU-to-FC2 producer fusion that
+ *      keeps the two reference BF16 boundaries): the gate value g and the up
+ *      value u are the bf16 FC1 outputs; h = bf16(silu(g) * u) with
+ *      silu(g) = g / (1 + e^-g), one rounding to bf16 of the real value.
  *
  * Build: gcc -std=c11 -O2 -fno-fast-math -ffp-contract=off -fopenmp
  *        -shared -fPIC  (strict IEEE fp32, no fused multiply-add contraction).
@@ -302,6 +306,61 @@ ORC_API void orc_dequantize(const uint8_t* codes, const uint8_t* sf, float gscal
             uint8_t q = (k % 2 == 0) ? (byte & 15u) : (byte >> 4);
             double S = orc_e4m3_decode(sf[orc_sf_offset(r, k / 16, K)]);
             out[r * K + k] = orc_e2m1_decode(q) * S * (double)gscale;
+        }
+}
+
+/* ------------------------------------------------------------------ */
+/* SwiGLU at the FC1 -> FC2 boundary (R8).                              */
+/* ------------------------------------------------------------------ */
+
+/* Round a finite double d to the nearest bf16 (8 significant bits;
+ * subnormals on the 2^-133 grid; overflow past the largest finite bf16 gives
+ * infinity, as in fp32 -> bf16).  `dir` is the sign of (true value - d) when d
+ * is only the leading part of the value being rounded: an exact midpoint then
+ * goes to the side the true value lies on; with dir = 0 ties go to even. */
+static uint16_t bf16_round(double d, int dir)
+{
+    uint16_t sign = signbit(d) ? 0x8000u : 0u;
+    double a = fabs(d);
+    if (a == 0.0) return sign;
+    int e;
+    (void)frexp(a, &e);           /* a = f * 2^e, f in [0.5, 1) */
+    int q = e - 8;                /* quantum of an 8-bit significand */
+    if (q < -133) q = -133;       /* bf16 subnormal spacing */
+    double x = ldexp(a, -q);      /* exact: the bf16 grid becomes the integers */
+    double n = nearbyint(x);      /* default rounding mode: nearest, ties to even */
+    if (dir != 0 && x - floor(x) == 0.5) {
+        int up = (dir > 0) == (sign == 0);  /* the true magnitude lies above a */
+        n = up ? ceil(x) : floor(x);
+    }
+    float r = (float)ldexp(n, q); /* exact in fp32 unless it overflows */
+    return (uint16_t)(sign | (bits_from_f32(r) >> 16));
+}
+
+ORC_API uint16_t orc_swiglu_bf16(uint16_t g, uint16_t u)
+{
+    double gd = (double)orc_bf16_to_float(g), ud = (double)orc_bf16_to_float(u);
+    if (fabs(gd) < 0x1p-30) {
+        /* silu(g) = g/2 + g^2/4 + O(g^4).  (g/2) * u is exact in double (two
+         * 8-bit significands); the remainder (g^2/4) * u is far below every
+         * bf16 spacing but has the sign of u, which decides exact midpoints. */
+        int dir = (gd == 0.0 || ud == 0.0) ? 0 : (ud > 0.0 ? 1 : -1);
+        return bf16_round(0.5 * gd * ud, dir);
+    }
+    double silu = gd / (1.0 + exp(-gd));
+    return bf16_round(silu * ud, 0);
+}
+
+/* Elementwise over an FC1 output in the SwiGLU row layout: y [rows][2*H] holds,
+ * for every group t of 128 hidden units, the 128 gate columns [256 t, 256 t + 128)
+ * followed by the matching 128 up columns; h [rows][H]. */
+ORC_API void orc_swiglu_rows(const uint16_t* y, int64_t rows, int64_t H, uint16_t* h)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t j = 0; j < H; ++j) {
+            int64_t t = j / 128, i = j % 128;
+            h[r * H + j] = orc_swiglu_bf16(y[r * 2 * H + 256 * t + i], y[r * 2 * H + 256 * t + 128 + i]);
         }
 }
 

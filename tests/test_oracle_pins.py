@@ -408,3 +408,88 @@ def test_quantize_gscale_given_and_segments(orc):
     # one global amax spans both segments
     m = orc.modulate(d["x"], d["shift"], d["scale"], d["seg_off"])
     assert g1 == orc.global_scale(orc.amax(m))
+
+
+# ------------------------------------------------------------------ SwiGLU producer
+
+def _bf16_value(bits):
+    return Fraction(float(np.array([bits << 16], np.uint32).view(np.float32)[0]))
+
+
+def _nearest_bf16(v: Fraction) -> int:
+    """Correctly rounded bf16 (ties to even) of an exact rational, by comparing
+    exact distances to the two bf16 neighbours of its fp32 approximation."""
+    if v == 0:
+        return 0
+    sign = 0x8000 if v < 0 else 0
+    a = abs(v)
+    f32 = np.float32(float(a))
+    lo = int(np.array([f32], np.float32).view(np.uint32)[0]) >> 16
+    best = None
+    for b in (lo - 1, lo, lo + 1, lo + 2):
+        if b < 0 or b >= 0x7F80:
+            continue
+        dist = abs(_bf16_value(b) - a)
+        key = (dist, b & 1)          # nearer first; on a tie the even code
+        if best is None or key < best[0]:
+            best = (key, b)
+    return sign | best[1]
+
+
+def _exact_swiglu(g_bits, u_bits, prec=60):
+    """silu(g) * u with 60-digit decimal arithmetic (its own exp), as a Fraction."""
+    from decimal import Decimal, localcontext
+    g, u = _bf16_value(g_bits), _bf16_value(u_bits)
+    with localcontext() as ctx:
+        ctx.prec = prec
+        gd = Decimal(g.numerator) / Decimal(g.denominator)
+        ud = Decimal(u.numerator) / Decimal(u.denominator)
+        val = gd / (1 + (-gd).exp()) * ud
+    return Fraction(val)
+
+
+def test_swiglu_matches_high_precision_rounding(orc):
+    """bf16(silu(g) * u) against 60-digit decimal arithmetic and an exact
+    nearest-bf16 search, over every bf16 g in [-24, 24] with a spread of u."""
+    rng = np.random.default_rng(7)
+    gs = [b for b in range(0x10000) if (b & 0x7F80) != 0x7F80 and abs(_bf16_value(b)) <= 24]
+    gs = [gs[i] for i in rng.choice(len(gs), 3000, replace=False)] + [0x0000, 0x8000, 0x3F80, 0xBF80]
+    gs += [0x0001, 0x8001, 0x00B9, 0x8093, 0x2570, 0xA570, 0x3000, 0xB000]   # tiny |g|: near-midpoints
+    us = [0x3F80, 0xBF80, 0x4049, 0x3C23, 0xC2F7]
+    bad = []
+    for i, g in enumerate(gs):
+        u = us[i % len(us)] if i % 3 else int(rng.integers(0x3000, 0x4300)) | (0x8000 if i % 2 else 0)
+        want = _nearest_bf16(_exact_swiglu(g, u))
+        got = orc.swiglu_bf16(g, u)
+        if want & 0x7FFF == 0:       # an exact zero keeps the IEEE product sign
+            want = (g ^ u) & 0x8000 if (g & 0x7FFF) == 0 else want
+        if got != want:
+            bad.append((hex(g), hex(u), hex(got), hex(want)))
+    assert not bad, bad[:10]
+
+
+def test_swiglu_closed_forms(orc):
+    for u in (0x3F80, 0xBF80, 0x4120):
+        h = orc.swiglu_bf16(0x0000, u)                 # silu(0) = 0
+        assert h & 0x7FFF == 0
+    # g >= 128: e^-g < 2^-184, so h = bf16(g * u), the rounded exact product
+    for g in (0x4300, 0x4349, 0x4400):
+        for u in (0x3F80, 0x3FC0, 0xC0A0):
+            assert orc.swiglu_bf16(g, u) == _nearest_bf16(_bf16_value(g) * _bf16_value(u))
+    # g <= -128: |silu(g) * u| < 1e-50, far below the smallest bf16: a signed zero
+    assert orc.swiglu_bf16(0xC300, 0x3F80) == 0x8000
+    assert orc.swiglu_bf16(0xC300, 0xBF80) == 0x0000
+
+
+def test_swiglu_rows_pairing(orc):
+    """Row layout: in each 256-column group the first 128 columns are gates and
+    the next 128 the matching ups; h column 128 t + i pairs y columns
+    256 t + i and 256 t + 128 + i."""
+    rng = np.random.default_rng(3)
+    y = W.to_bf16_bits(rng.standard_normal((5, 512)).astype(np.float32))
+    h = orc.swiglu_rows(y)
+    assert h.shape == (5, 256)
+    for r in range(5):
+        for j in range(256):
+            t, i = divmod(j, 128)
+            assert h[r, j] == orc.swiglu_bf16(int(y[r, 256 * t + i]), int(y[r, 256 * t + 128 + i]))
