@@ -18,6 +18,7 @@ import torch
 
 __all__ = [
     "H3FP4Error", "PROLOGUE_MOD", "EPI_BIAS", "EPI_GATE_RESID", "GSCALE_GIVEN", "A_PREQUANT",
+    "EPI_SWIGLU", "EPI_AMAX", "h3fp4_ws_out_amax",
     "MAX_SEGMENTS", "library_path", "load_library", "h3fp4_codes_bytes", "h3fp4_sf_bytes",
     "h3fp4_workspace_bytes", "h3fp4_quantize_weight", "h3fp4_quantize_act", "h3fp4_linear",
     "h3fp4_check", "h3fp4_act_amax", "h3fp4_gscale_from_amax", "h3fp4_selftest_timeout", "h3fp4_measure_fp4_peak", "h3fp4_measure_fp4_pair_peak", "h3fp4_quantize_act_noalloc",
@@ -29,6 +30,8 @@ EPI_BIAS = 2
 EPI_GATE_RESID = 4
 GSCALE_GIVEN = 16
 A_PREQUANT = 32
+EPI_SWIGLU = 64
+EPI_AMAX = 128
 MAX_SEGMENTS = 8
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -65,6 +68,7 @@ def load_library():
                                i32, vp, vp]),
         "h3fp4_act_amax": (i32, [vp, i64, i64, vp, vp, vp, i32, vp, i32, vp, vp]),
         "h3fp4_gscale_from_amax": (i32, [vp, vp, vp]),
+        "h3fp4_ws_out_amax": (vp, [vp]),
         "h3fp4_selftest_timeout": (i32, [vp, C.c_uint64, vp]),
         "h3fp4_measure_fp4_peak": (i32, [i32, vp, vp]),
         "h3fp4_measure_fp4_pair_peak": (i32, [i32, vp, vp]),
@@ -166,19 +170,23 @@ def h3fp4_linear(x: torch.Tensor, w_codes: torch.Tensor, w_sf: torch.Tensor, w_g
                  shift: Optional[torch.Tensor] = None, scale: Optional[torch.Tensor] = None,
                  gate: Optional[torch.Tensor] = None, resid: Optional[torch.Tensor] = None,
                  bias: Optional[torch.Tensor] = None, seg_off: Optional[Sequence[int]] = None,
-                 gscale_given: bool = False, stream=None) -> None:
+                 gscale_given: bool = False, swiglu: bool = False, out_amax: bool = False,
+                 stream=None) -> None:
     """out = [R + g*](alpha * NVFP4(prologue(x)) . W^T [+ b]).
 
     ``x`` is bf16 [M, K]; or uint8 codes [M, K/2] together with ``a_sf`` and
-    ``a_gscale`` (pre-quantised activation).
+    ``a_gscale`` (pre-quantised activation).  ``swiglu``: out is [M, N/2] =
+    bf16(silu(g) * u) over the weight's [gate 128 | up 128] row groups.
+    ``out_amax``: also leave max|out| at :func:`h3fp4_ws_out_amax` (ws).
     """
     prequant = x.dtype == torch.uint8
     M = x.shape[0]
     K = x.shape[1] * (2 if prequant else 1)
-    N = out.shape[1]
+    N = out.shape[1] * (2 if swiglu else 1)
     flags = ((A_PREQUANT if prequant else 0) | (PROLOGUE_MOD if shift is not None else 0)
              | (EPI_BIAS if bias is not None else 0) | (EPI_GATE_RESID if gate is not None else 0)
-             | (GSCALE_GIVEN if gscale_given else 0))
+             | (GSCALE_GIVEN if gscale_given else 0) | (EPI_SWIGLU if swiglu else 0)
+             | (EPI_AMAX if out_amax else 0))
     sp, nseg, _keep = _segs(seg_off)
     _check(load_library().h3fp4_linear(
         _ptr(x, "x"), _ptr(a_sf, "a_sf", torch.uint8), _ptr(a_gscale, "a_gscale", torch.float32), M, N, K,
@@ -218,6 +226,13 @@ def h3fp4_act_amax(x: torch.Tensor, amax: torch.Tensor, ws: torch.Tensor, shift:
         _ptr(scale, "scale", torch.float32), sp, nseg, _ptr(amax, "amax", torch.float32),
         PROLOGUE_MOD if shift is not None else 0, _ptr(ws, "ws", torch.uint8), _stream(stream)),
         "h3fp4_act_amax")
+
+
+def h3fp4_ws_out_amax(ws: torch.Tensor) -> torch.Tensor:
+    """The fp32 [1] view of ``ws`` where an ``out_amax`` linear leaves max|out|."""
+    addr = load_library().h3fp4_ws_out_amax(_ptr(ws, "ws", torch.uint8))
+    off = int(addr) - ws.data_ptr()
+    return ws[off:off + 4].view(torch.float32)
 
 
 def h3fp4_gscale_from_amax(amax: torch.Tensor, gscale: torch.Tensor, stream=None) -> None:

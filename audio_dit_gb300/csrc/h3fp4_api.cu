@@ -76,7 +76,7 @@ cudaError_t ensure_dynamic_smem(const void* func, int bytes)
         int dev;
     };
     static std::mutex mu;
-    static Entry done[4 * kMaxDevices];
+    static Entry done[16 * kMaxDevices];
     static int ndone = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -85,7 +85,7 @@ cudaError_t ensure_dynamic_smem(const void* func, int bytes)
     for (int i = 0; i < ndone; ++i)
         if (done[i].func == func && done[i].dev == dev) return cudaSuccess;
     e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess && ndone < 4 * kMaxDevices) done[ndone++] = Entry{func, dev};
+    if (e == cudaSuccess && ndone < 16 * kMaxDevices) done[ndone++] = Entry{func, dev};
     return e;
 }
 
@@ -188,13 +188,17 @@ h3fp4_status h3fp4_linear(const void* x, const void* a_sf, const float* a_gscale
     if (st != H3FP4_OK) return st;
     if (N < 8 || N % 8 != 0 || N > (int64_t)INT32_MAX) return H3FP4_ERR_SHAPE;
     const int known = H3FP4_PROLOGUE_MOD | H3FP4_EPI_BIAS | H3FP4_EPI_GATE_RESID | H3FP4_GSCALE_GIVEN |
-                      H3FP4_A_PREQUANT;
+                      H3FP4_A_PREQUANT | H3FP4_EPI_SWIGLU | H3FP4_EPI_AMAX;
     if (flags & ~known) return H3FP4_ERR_INVALID;
     const bool prequant = (flags & H3FP4_A_PREQUANT) != 0;
     const bool mod = (flags & H3FP4_PROLOGUE_MOD) != 0;
     const bool bias = (flags & H3FP4_EPI_BIAS) != 0;
     const bool gated = (flags & H3FP4_EPI_GATE_RESID) != 0;
     const bool given = (flags & H3FP4_GSCALE_GIVEN) != 0;
+    const bool swiglu = (flags & H3FP4_EPI_SWIGLU) != 0;
+    const bool want_amax = (flags & H3FP4_EPI_AMAX) != 0;
+    if (swiglu && N % 256 != 0) return H3FP4_ERR_SHAPE;
+    if (swiglu && gated) return H3FP4_ERR_INVALID;
     if (!x || !w_codes || !w_sf || !w_gscale || !out_bf16 || !ws) return H3FP4_ERR_INVALID;
     if (prequant && (mod || !a_sf || !a_gscale)) return H3FP4_ERR_INVALID;
     if (given && !a_gscale) return H3FP4_ERR_INVALID;
@@ -212,6 +216,10 @@ h3fp4_status h3fp4_linear(const void* x, const void* a_sf, const float* a_gscale
     if ((st = check_device()) != H3FP4_OK) return st;
 
     uint8_t* wsb = static_cast<uint8_t*>(ws);
+    // Zeroed ahead of the quantiser so that the quantiser -> GEMM launch pair
+    // stays adjacent (programmatic dependent launch).
+    if (want_amax && (st = from_cuda(cudaMemsetAsync(wsb + kWsOutAmax, 0, sizeof(float), stream))) != H3FP4_OK)
+        return st;
     GemmJob g{};
     if (prequant) {
         g.a_codes = static_cast<const uint8_t*>(x);
@@ -248,7 +256,14 @@ h3fp4_status h3fp4_linear(const void* x, const void* a_sf, const float* a_gscale
     g.seg = seg;
     g.status = reinterpret_cast<unsigned int*>(wsb + kWsStatus);
     g.wait_limit_ns = g_wait_limit_ns.load();
+    g.swiglu = swiglu;
+    g.amax_out = want_amax ? reinterpret_cast<float*>(wsb + kWsOutAmax) : nullptr;
     return from_cuda(launch_gemm(g, stream));
+}
+
+float* h3fp4_ws_out_amax(void* ws)
+{
+    return ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWsOutAmax) : nullptr;
 }
 
 h3fp4_status h3fp4_act_amax(const void* x_bf16, int64_t M, int64_t K, const float* shift, const float* scale,

@@ -113,6 +113,7 @@ struct GemmParams {
     unsigned int* status;
     unsigned long long wait_ns;
     int stall;  // self-test: the producer issues nothing, so every consumer wait must time out
+    float* amax_out;  // kAmax: atomic max of |out| (bf16 values, as fp32 bits) over the call
 };
 
 __device__ __forceinline__ int segment_of_row(const Segments& s, int r)
@@ -131,6 +132,8 @@ __device__ __forceinline__ uint32_t swz64(uint32_t r, uint32_t j)
     return lin ^ (((lin >> 7) & 3u) << 4);
 }
 
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
@@ -138,6 +141,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return l | (h << 16);
 }
 
+// kSwiglu: SwiGLU epilogue (out [M][N/2]); kAmax: track max |out| into p.amax_out.
+// Compile-time, so that the plain epilogue carries neither.
+template <bool kSwiglu, bool kAmax>
 __global__ void __launch_bounds__(kThreads, 1)
     nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -368,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float alpha = __fmul_rn(__ldg(p.a_gscale), __ldg(p.w_gscale));
         uint32_t acc_phase = 0, r_phase = 0;
         bool r_pending = false;
+        float omax = 0.0f;  // max |out| over this lane's rows < M (before the bf16 rounding)
         for (int tile = blockIdx.x >> 1; tile < num_tiles; tile += gridDim.x >> 1) {
             if (__any_sync(0xffffffffu, s_abort != 0)) break;  // warp-uniform exit
             const int mp = tile / p.n_tiles, nt = tile - mp * p.n_tiles;
@@ -392,9 +399,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc_phase ^= 1u;
             tc_fence_after();
             uint32_t acc[4][32];
-            const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + 128u * h;
+            // Plain: this warp's columns [128 h, +128) in acc[0..3].  SwiGLU: the
+            // gate columns [64 h, +64) in acc[0..1] and the matching up columns
+            // [128 + 64 h, +64) in acc[2..3].
+            const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tc_ld_32x32b_x32(tbase + 32u * c, acc[c]);
+            for (int c = 0; c < 4; ++c) {
+                const uint32_t col = kSwiglu ? 64u * h + 128u * (c >> 1) + 32u * (c & 1) : 128u * h + 32u * c;
+                tc_ld_32x32b_x32(tq + col, acc[c]);
+            }
             tc_wait_ld();
             tc_fence_before();
             __syncwarp();
@@ -406,6 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool failed = false;
 #pragma unroll
             for (int pass = 0; pass < 2; ++pass) {
+                if (pass == 1 && kSwiglu) break;  // 64 output columns per warp: one pass
                 if (pass == 1) {
                     if (lane == 0) bulk_wait_read_all();  // pass 0's stores have read the buffers
                     __syncwarp();
@@ -429,6 +443,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int cc = 0; cc < 2; ++cc) {
                     const int c = 2 * pass + cc;
                     uint8_t* buf = stg + cc * kChunkBytes;
+                    if constexpr (kSwiglu) {
+                        // g, u = the plain epilogue's values rounded to bf16 (the FC1
+                        // output boundary); h = bf16(silu(g) * u) in fp32.
+                        const int ng = nt * BN + 64 * h + 32 * cc;  // gate column of the chunk (up: + 128)
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            float bg[8], bu[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                bg[i] = 0.0f;
+                                bu[i] = 0.0f;
+                            }
+                            if (p.bias != nullptr) {
+                                const uint4 gv = __ldg(reinterpret_cast<const uint4*>(p.bias + ng + 8 * j));
+                                const uint4 uv = __ldg(reinterpret_cast<const uint4*>(p.bias + ng + 128 + 8 * j));
+                                const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w}, uw[4] = {uv.x, uv.y, uv.z, uv.w};
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    bg[2 * i] = __uint_as_float(gw[i] << 16);
+                                    bg[2 * i + 1] = __uint_as_float(gw[i] & 0xFFFF0000u);
+                                    bu[2 * i] = __uint_as_float(uw[i] << 16);
+                                    bu[2 * i + 1] = __uint_as_float(uw[i] & 0xFFFF0000u);
+                                }
+                            }
+                            float o[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const float g = bf16_round(
+                                    __fadd_rn(__fmul_rn(__uint_as_float(acc[cc][8 * j + i]), alpha), bg[i]));
+                                const float u = bf16_round(
+                                    __fadd_rn(__fmul_rn(__uint_as_float(acc[2 + cc][8 * j + i]), alpha), bu[i]));
+                                o[i] = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+                                if (kAmax && row < p.M) omax = fmaxf(omax, fabsf(o[i]));
+                            }
+                            *reinterpret_cast<uint4*>(buf + swz64(lane, j)) =
+                                make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                                           pack_bf16x2(o[6], o[7]));
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) tma_store_2d(&tmOut, buf, nt * (BN / 2) + 64 * h + 32 * cc, m0);
+                        continue;
+                    } else {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int n8 = nc0 + 32 * c + 8 * j;
@@ -472,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float y = __fmul_rn(__uint_as_float(acc[c][8 * j + i]), alpha);
                             const float v = __fadd_rn(y, b[i]);
                             o[i] = (grow != nullptr) ? __fmaf_rn(g[i], v, r[i]) : __fadd_rn(v, r[i]);
+                            if (kAmax && row < p.M && n8 < p.N) omax = fmaxf(omax, fabsf(o[i]));
                         }
                         *slot = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
                                            pack_bf16x2(o[6], o[7]));
@@ -479,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) tma_store_2d(&tmOut, buf, nc0 + 32 * c, m0);
+                    }
                 }
                 if (lane == 0) bulk_commit();
             }
@@ -488,6 +547,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (r_pending) (void)mbar_wait(&rbar[e], r_phase, p.wait_ns, p.status, kStatusTimeoutEpilogue);
+        if constexpr (kAmax) {
+            // bf16 rounding is monotone and odd, so the largest stored |out| is
+            // the rounded largest |out|; non-negative floats order like their bits.
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) omax = fmaxf(omax, __shfl_xor_sync(0xffffffffu, omax, off));
+            if (lane == 0) atomicMax(reinterpret_cast<unsigned int*>(p.amax_out), __float_as_uint(bf16_round(omax)));
+        }
         if (lane == 0) bulk_wait_all();
         __syncwarp();
     }
@@ -570,7 +636,7 @@ static int max_pairs_current_device()
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel, &cfg) != cudaSuccess || n <= 0)
+        if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel<false, false>, &cfg) != cudaSuccess || n <= 0)
             n = sm_count_current_device() / 2;
         cache[dev] = n;
     }
@@ -586,6 +652,7 @@ static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t 
     const int64_t kb4 = job.K / 64;
     // Block scales as rows of 256 bytes: one 512-byte tile is two rows.
     const uint64_t sfa_rows = (uint64_t)(m_tiles * kb4 * 2), sfb_rows = (uint64_t)(n_sf_tiles * kb4 * 2);
+    const uint64_t out_cols = job.swiglu ? (uint64_t)job.N / 2 : (uint64_t)job.N;
     if (!make_map_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, job.a_codes, kbytes, (uint64_t)job.M, kbytes, BK / 2, BM,
                      CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, job.w_codes, kbytes, (uint64_t)job.N, kbytes, BK / 2,
@@ -594,8 +661,8 @@ static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t 
                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map_2d(&tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, job.w_sf, 256, sfb_rows, 256, 256, kSfBox / 256,
                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map_2d(&tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, job.out, (uint64_t)job.N, (uint64_t)job.M,
-                     (uint64_t)job.N * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_map_2d(&tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, job.out, out_cols, (uint64_t)job.M, out_cols * 2, 32,
+                     32, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map_2d(&tmR, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, job.resid ? job.resid : job.out, (uint64_t)job.N,
                      (uint64_t)job.M, (uint64_t)job.N * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
@@ -618,8 +685,11 @@ static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t 
     p.status = job.status;
     p.wait_ns = job.wait_limit_ns;
     p.stall = stall;
+    p.amax_out = job.amax_out;
 
-    const cudaError_t attr_err = ensure_dynamic_smem(reinterpret_cast<const void*>(nvfp4_gemm_kernel), (int)kSmemBytes);
+    auto kernel = job.swiglu ? (job.amax_out ? nvfp4_gemm_kernel<true, true> : nvfp4_gemm_kernel<true, false>)
+                             : (job.amax_out ? nvfp4_gemm_kernel<false, true> : nvfp4_gemm_kernel<false, false>);
+    const cudaError_t attr_err = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), (int)kSmemBytes);
     if (attr_err != cudaSuccess) return attr_err;
 
     const int tiles = p.pair_m_tiles * p.n_tiles;
@@ -640,7 +710,7 @@ static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t 
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, nvfp4_gemm_kernel, tmA, tmB, tmSFA, tmSFB, tmOut, tmR, p);
+    return cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmSFA, tmSFB, tmOut, tmR, p);
 }
 
 }  // namespace h3fp4

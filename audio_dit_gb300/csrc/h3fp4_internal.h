@@ -12,6 +12,7 @@ constexpr size_t kWsStatus = 0;         // uint32 device status word (+ padding)
 constexpr size_t kWsPartials = 256;     // fp32 amax partial maxima
 constexpr int kMaxPartials = 4096;
 constexpr size_t kWsActGscale = kWsPartials + 4 * kMaxPartials;  // fp32 activation global scale
+constexpr size_t kWsOutAmax = kWsActGscale + 16;                  // fp32 max |out| of the last EPI_AMAX call
 constexpr size_t kWsActCodes = kWsActGscale + 256;                // activation codes, then block scales
 
 // Device status bits (workspace status word).
@@ -52,10 +53,12 @@ struct GemmJob {
     const void* bias;        // bf16 [N] or null
     const float* gate;       // fp32 [nseg][N] or null
     const void* resid;       // bf16 [M][N] or null
-    void* out;               // bf16 [M][N]
+    void* out;               // bf16 [M][N], or [M][N/2] with swiglu
     Segments seg;
     unsigned int* status;    // device status word
     uint64_t wait_limit_ns;
+    bool swiglu;             // SwiGLU epilogue (N % 256 == 0, no gate/residual)
+    float* amax_out;         // zeroed by the caller; receives max |out| (or null)
 };
 
 cudaError_t launch_gemm(const GemmJob& job, cudaStream_t s);

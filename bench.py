@@ -176,6 +176,70 @@ class Problem:
         return b
 
 
+def time_mlp_chain(torch, A, steps: int, warmup: int, flush):
+    """MLP FC1 -> SwiGLU -> FC2 through the public call, X [32768, 3072] with the
+    fc1 recipe and modulation, W1 [24576, 3072] in [gate 128 | up 128] row groups,
+    h [32768, 12288], then the fc2 weights, gate and residual. FC1's epilogue
+    writes h = bf16(silu(g) * u) and max|h|; FC2 quantises h in one pass with the
+    global scale derived from it. For comparison the same FC2 also runs with its
+    own two-pass (in-run amax) quantisation of h."""
+    import workloads as W
+    M = 32768
+    d1 = W.swiglu_fc1_inputs(M)
+    d2 = W.make_inputs("fc2", M=M, with_x=False)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda()
+    N1, K1, N2, K2 = d1["N"], d1["K"], d2["N"], d2["K"]
+    x, b1, sh, sc = dev(d1["x"]), dev(d1["bias"]), f32(d1["shift"]), f32(d1["scale"])
+    ws1 = A.alloc_workspace(max(M, N1), N1, K1, 0)
+    wq1 = A.alloc_nvfp4(N1, K1)
+    A.h3fp4_quantize_weight(dev(d1["w"]), *wq1, ws1)
+    ws2 = A.alloc_workspace(max(M, N2), N2, K2, 0)
+    wq2 = A.alloc_nvfp4(N2, K2)
+    A.h3fp4_quantize_weight(dev(d2["w"]), *wq2, ws2)
+    b2, g2, r2 = dev(d2["bias"]), f32(d2["gate"]), dev(d2["resid"])
+    h = torch.empty((M, N1 // 2), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((M, N2), dtype=torch.bfloat16, device="cuda")
+    gs2 = torch.empty(1, dtype=torch.float32, device="cuda")
+    amax = A.h3fp4_ws_out_amax(ws1)
+    s = torch.cuda.current_stream()
+
+    def fc1():
+        A.h3fp4_linear(x, *wq1, h, ws1, shift=sh, scale=sc, bias=b1, swiglu=True, out_amax=True)
+
+    def fc2(given):
+        if given:
+            A.h3fp4_gscale_from_amax(amax, gs2)
+        A.h3fp4_linear(h, *wq2, out, ws2, a_gscale=gs2 if given else None, gscale_given=given,
+                       bias=b2, gate=g2, resid=r2)
+
+    for _ in range(warmup):
+        flush(); fc1(); fc2(True); fc2(False)
+    torch.cuda.synchronize()
+    t1, t2, t2b = [], [], []
+    for _ in range(steps):
+        flush()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record(s); fc1(); e[1].record(s); fc2(True); e[2].record(s)
+        flush()
+        f = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        f[0].record(s); fc2(False); f[1].record(s)
+        torch.cuda.synchronize()
+        t1.append(e[0].elapsed_time(e[1])); t2.append(e[1].elapsed_time(e[2])); t2b.append(f[0].elapsed_time(f[1]))
+    A.h3fp4_check(ws1)
+    A.h3fp4_check(ws2)
+    flops = 2.0 * M * K1 * N1 + 2.0 * M * K2 * N2
+    step = float(np.mean(t1) + np.mean(t2))
+    res = {"tflops": round(flops / (step * 1e-3) / 1e12, 1), "ms_per_step": round(step, 4),
+           "fc1_swiglu_ms": round(float(np.mean(t1)), 4),
+           "fc2_producer_amax_ms": round(float(np.mean(t2)), 4),
+           "fc2_two_pass_ms": round(float(np.mean(t2b)), 4),
+           "shape": f"X [{M},{K1}] -> FC1 [{N1},{K1}] + SwiGLU -> h [{M},{N1 // 2}] -> FC2 [{N2},{K2}] + gate/resid"}
+    del x, h, out, r2, ws1, ws2, wq1, wq2
+    torch.cuda.empty_cache()
+    return res
+
+
 def time_device_steps(torch, A, prob: Problem, steps: int, warmup: int, flush, given_scale: bool = False):
     """Per-step CUDA events on the launching stream: [quant | gemm], L2 flushed
     between steps. With given_scale the quantisation is the pack pass alone
@@ -411,6 +475,10 @@ def run_gpu(args):
                 torch.cuda.empty_cache()
             except Exception as e:  # a failing extra config must not hide the headline
                 extra[name] = {"error": repr(e)[:200]}
+        try:
+            extra["mlp_swiglu"] = time_mlp_chain(torch, A, max(3, min(50, args.steps // 40)), 3, flush)
+        except Exception as e:
+            extra["mlp_swiglu"] = {"error": repr(e)[:200]}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -93,7 +93,9 @@ enum {
     H3FP4_EPI_BIAS = 2,        /* add bias[n] (bf16)                                               */
     H3FP4_EPI_GATE_RESID = 4,  /* out = R[m][n] + gate[seg][n] * v   (gate fp32 [nseg][N])         */
     H3FP4_GSCALE_GIVEN = 16,   /* activation global scale read from a_gscale (device fp32 > 0)     */
-    H3FP4_A_PREQUANT = 32      /* x is already NVFP4: codes + a_sf + a_gscale                     */
+    H3FP4_A_PREQUANT = 32,     /* x is already NVFP4: codes + a_sf + a_gscale                     */
+    H3FP4_EPI_SWIGLU = 64,     /* out[M][N/2] = bf16(silu(g) * u), see h3fp4_linear                */
+    H3FP4_EPI_AMAX = 128       /* also write max|out| to h3fp4_ws_out_amax(ws)                    */
 };
 
 #define H3FP4_MAX_SEGMENTS 8
@@ -144,7 +146,26 @@ H3FP4_API h3fp4_status h3fp4_quantize_act(const void* x_bf16, int64_t M, int64_t
  *   shift/scale: as in h3fp4_quantize_act (with H3FP4_PROLOGUE_MOD).
  *   gate: fp32 [nseg][N] and resid: bf16 [M][N], with H3FP4_EPI_GATE_RESID.
  *   bias: bf16 [N], with H3FP4_EPI_BIAS.
- *   out may not alias x, resid or the weights. */
+ *   out may not alias x, resid or the weights.
+ *
+ * SwiGLU producer (H3FP4_EPI_SWIGLU; "H3 Runtime Current State", "Owned
+ * Performance Kernels": the exact SwiGLU-to-FC2 NVFP4 producer fusion that
+ * keeps the two reference BF16 boundaries).  N % 256 == 0, and the weight
+ * rows (and bias) come in groups of 256: rows [256 t, 256 t + 128) are the
+ * gate rows and rows [256 t + 128, 256 t + 256) the up rows of hidden units
+ * [128 t, 128 t + 128).  With g, u the bf16 outputs the plain epilogue would
+ * write for a gate and its up row (the FC1 output boundary),
+ *     out[m][128 t + i] = bf16(silu(g) * u),  silu(g) = g / (1 + e^-g),
+ * evaluated in fp32 (IEEE divide, CUDA expf); out is [M][N/2].  Not with
+ * H3FP4_EPI_GATE_RESID.
+ *
+ * Output amax (H3FP4_EPI_AMAX; "H3 Blackwell Runtime Plan", "Next Performance
+ * Plan: Blackwell NVFP4 GEMMs": scale discovery): the call also stores
+ * max |out| over all M rows of its bf16 output, as fp32, at
+ * h3fp4_ws_out_amax(ws).  A following h3fp4_gscale_from_amax and
+ * H3FP4_GSCALE_GIVEN quantisation of `out` (no prologue) then produce the
+ * same codes, block scales and global scale as the two-pass quantisation,
+ * with one pass over `out` instead of two. */
 H3FP4_API h3fp4_status h3fp4_linear(const void* x, const void* a_sf, const float* a_gscale,
                           int64_t M, int64_t N, int64_t K,
                           const void* w_codes, const void* w_sf, const float* w_gscale,
@@ -189,6 +210,11 @@ H3FP4_API h3fp4_status h3fp4_act_amax(const void* x_bf16, int64_t M, int64_t K,
                                       const float* shift, const float* scale,
                                       const int64_t* seg_off, int nseg,
                                       float* amax, int flags, void* ws, cudaStream_t stream);
+
+/* Device address inside the workspace where an H3FP4_EPI_AMAX call of
+ * h3fp4_linear leaves max|out| (fp32); valid until the workspace's next
+ * EPI_AMAX call.  NULL for a NULL workspace.  No device access. */
+H3FP4_API float* h3fp4_ws_out_amax(void* ws);
 
 /* *gscale = (*amax == 0) ? 1 : *amax / (6*448), on the device (one thread). */
 H3FP4_API h3fp4_status h3fp4_gscale_from_amax(const float* amax, float* gscale, cudaStream_t stream);

@@ -64,7 +64,24 @@ def test_host_validation_rejects_before_launch(lib):
     # unknown flag bits
     assert lib.h3fp4_linear(dummy, None, None, 16, 16, 64, dummy, dummy, dummy, None, None, None, None, 1,
                             None, None, dummy, 1 << 10, dummy, None) == 1
+    # SwiGLU epilogue: N must be a whole number of 256-row [gate | up] groups,
+    # and it does not combine with the residual gate
+    assert lib.h3fp4_linear(dummy, None, None, 16, 264, 64, dummy, dummy, dummy, None, None, None, None, 1,
+                            None, None, dummy, 64, dummy, None) == 2
+    assert lib.h3fp4_linear(dummy, None, None, 16, 256, 64, dummy, dummy, dummy, None, None, dummy, None, 1,
+                            None, dummy, dummy, 64 | 4, dummy, None) == 1
     assert lib.h3fp4_status_string(5) == b"device wait timed out"
+
+
+def test_ws_out_amax_address(lib):
+    import audio_dit_gb300 as A
+    lib.h3fp4_ws_out_amax.restype = C.c_void_p
+    base = 1 << 20
+    addr = lib.h3fp4_ws_out_amax(C.c_void_p(base))
+    # inside the workspace, 4-byte aligned, ahead of the activation codes
+    assert addr is not None and base < addr and addr % 4 == 0
+    assert addr + 4 <= base + A.h3fp4_workspace_bytes(1, 8, 64, A.A_PREQUANT)
+    assert lib.h3fp4_ws_out_amax(None) is None
 
 
 def test_product_does_not_touch_oracle():

@@ -1,0 +1,118 @@
+"""GPU parity of the SwiGLU producer epilogue and the output amax.
+
+SwiGLU: the epilogue's h = bf16(silu(g) * u) must equal the oracle's SwiGLU of
+the plain epilogue's own bf16 output (same inputs, same GPU), element by element:
+every element within one bf16 ulp and at least 99.9 % bit-identical (the GPU
+evaluates silu in fp32 with CUDA's expf, the oracle in float64; they can round a
+value lying within ~1e-6 of a bf16 midpoint differently).  The plain output
+itself is held to the float64 oracle by test_gpu_linear.
+
+Output amax: the stored value must be exactly max |out| of the bf16 output, and
+quantising `out` with the global scale derived from it must give the same codes,
+block scales and global scale as the two-pass quantisation of `out`.
+"""
+import numpy as np
+import pytest
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA device", allow_module_level=True)
+
+from _gpu_helpers import LinearCase, assert_quant_equal, gpu_quantize, host_u16  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from audio_dit_gb300 import build
+    build.build()
+
+
+def _ulp_diff(a_u16, b_u16):
+    """Distance in bf16 steps between two arrays of finite bf16 bit patterns."""
+    def key(x):
+        x = x.astype(np.int64)
+        return np.where(x & 0x8000, -(x & 0x7FFF), x & 0x7FFF)
+    return np.abs(key(a_u16) - key(b_u16))
+
+
+def _run_pair(d, rows=None):
+    """Plain linear [M, N] and SwiGLU linear [M, N/2] (both with out_amax) on one case."""
+    import audio_dit_gb300 as A
+    case = LinearCase(d)
+    y = case.run(out_amax=True).clone()
+    amax_plain = A.h3fp4_ws_out_amax(case.ws).clone()
+    h = torch.empty((d["M"], d["N"] // 2), dtype=torch.bfloat16, device="cuda")
+    A.h3fp4_linear(case.x, *case.wq, h, case.ws, shift=case.shift, scale=case.scale, bias=case.bias,
+                   swiglu=True, out_amax=True)
+    A.h3fp4_check(case.ws)
+    amax_h = A.h3fp4_ws_out_amax(case.ws).clone()
+    torch.cuda.synchronize()
+    return case, y, h, amax_plain, amax_h
+
+
+def _check_swiglu(orc, y, h, rows=None):
+    yh = host_u16(y if rows is None else y[rows])
+    hh = host_u16(h if rows is None else h[rows])
+    ref = orc.swiglu_rows(yh)
+    d = _ulp_diff(hh, ref)
+    assert d.max() <= 1, f"{int((d > 1).sum())} SwiGLU outputs more than one bf16 step off"
+    exact = float((d == 0).mean())
+    assert exact >= 0.999, f"only {exact:.5f} of SwiGLU outputs bit-identical"
+    return exact
+
+
+def _check_amax(t, amax):
+    want = t.float().abs().max()
+    assert torch.equal(amax.cpu().view(torch.int32), want.cpu().reshape(1).view(torch.int32)), \
+        (float(amax), float(want))
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 512, 512), (1000, 1024, 3072), (129, 256, 64)])
+def test_swiglu_matches_plain_epilogue(orc, M, N, K):
+    d = W.swiglu_fc1_inputs(M, N, K)
+    _, y, h, amax_plain, amax_h = _run_pair(d)
+    _check_swiglu(orc, y, h)
+    _check_amax(y, amax_plain)
+    _check_amax(h, amax_h)
+
+
+def test_swiglu_full_size_sampled_rows(orc):
+    """FC1 at its full size (X [32768, 3072], W [24576, 3072]) -> h [32768, 12288]:
+    sampled rows (tile and pair edges included) against the oracle, the amax exactly."""
+    d = W.swiglu_fc1_inputs(32768)
+    _, y, h, _, amax_h = _run_pair(d)
+    rng = np.random.default_rng(11)
+    rows = np.unique(np.concatenate([rng.integers(0, 32768, 48), [0, 127, 128, 255, 256, 32767]]))
+    _check_swiglu(orc, y, h, torch.from_numpy(rows).cuda())
+    _check_amax(h, amax_h)
+
+
+def test_swiglu_chain_into_fc2_quantisation(orc):
+    """h quantised with the scale from the producer's amax equals the two-pass
+    quantisation of h (GPU and oracle), and the FC2 linear accepts it."""
+    import audio_dit_gb300 as A
+    d = W.swiglu_fc1_inputs(384, 512, 512)
+    case, _, h, _, amax_h = _run_pair(d)
+    gs = torch.empty(1, dtype=torch.float32, device="cuda")
+    A.h3fp4_gscale_from_amax(amax_h, gs)
+    hb = host_u16(h)
+    one_pass = gpu_quantize(hb, gscale=float(gs.cpu()[0]))
+    two_pass = gpu_quantize(hb)
+    assert_quant_equal(one_pass, two_pass, "one pass (producer amax) vs two passes")
+    assert_quant_equal(one_pass, orc.quantize(hb), "one pass vs oracle")
+    # the FC2 linear consuming h with the caller-given global scale
+    w2 = W.to_bf16_bits(np.random.default_rng(5).standard_normal((256, 256), dtype=np.float32) * np.float32(0.01))
+    from _gpu_helpers import dev_bf16
+    wq = A.alloc_nvfp4(256, 256)
+    ws2 = A.alloc_workspace(384, 256, 256, 0)
+    A.h3fp4_quantize_weight(dev_bf16(w2), *wq, ws2)
+    out_given = torch.empty((384, 256), dtype=torch.bfloat16, device="cuda")
+    out_amax = torch.empty_like(out_given)
+    A.h3fp4_linear(h, *wq, out_given, ws2, a_gscale=gs, gscale_given=True)
+    A.h3fp4_linear(h, *wq, out_amax, ws2)
+    A.h3fp4_check(ws2)
+    assert torch.equal(out_given.view(torch.int16), out_amax.view(torch.int16))

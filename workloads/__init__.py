@@ -109,7 +109,7 @@ def make_w(wl: Workload) -> np.ndarray:
     return to_bf16_bits(g.standard_normal((wl.N, wl.K), dtype=np.float32) * np.float32(std))
 
 
-def make_inputs(name: str, M: Optional[int] = None) -> dict:
+def make_inputs(name: str, M: Optional[int] = None, with_x: bool = True) -> dict:
     """All tensors of a workload (numpy, host).  ``M`` overrides the row count.
 
     Returns a dict with x (bf16 bits [M,K]), w (bf16 bits [N,K]),
@@ -122,7 +122,7 @@ def make_inputs(name: str, M: Optional[int] = None) -> dict:
     seg_off = segment_offsets(wl, M)
     nseg = len(seg_off) - 1
     out = dict(workload=wl, M=M, K=wl.K, N=wl.N, seg_off=seg_off)
-    out["x"] = make_x(wl, M)
+    out["x"] = make_x(wl, M) if with_x else None
     out["w"] = make_w(wl)
     out["bias"] = to_bf16_bits(rng_for(wl.base_seed, T_BIAS).standard_normal(wl.N, dtype=np.float32)
                                * np.float32(0.01))
@@ -157,4 +157,26 @@ def m_sweep_inputs(M: int) -> dict:
     out["scale"] = rng_for(base.base_seed, T_SCALE).standard_normal((1, 3072), dtype=np.float32) * np.float32(0.1)
     out["gate"] = rng_for(base.base_seed, T_GATE).uniform(0.0, 1.0, (1, 3072)).astype(np.float32)
     out["resid"] = to_bf16_bits(rng_for(base.base_seed, T_RESID).standard_normal((M, 3072), dtype=np.float32))
+    return out
+
+
+def swiglu_fc1_inputs(M: int, N: int = 24576, K: int = 3072) -> dict:
+    """FC1 feeding FC2 through SwiGLU: X [M, K] with the fc1 distributions and
+    modulation vectors, W [N, K] ~ N(0, 0.02^2) whose rows are read as groups of
+    256 (128 gate rows, then the 128 matching up rows), bias [N] ~ N(0, 0.01^2).
+    N = 24576 gives the hidden width 12288 that the fc2 workload consumes."""
+    base = WORKLOADS["fc1"]
+    wl = dataclasses.replace(base, name="fc1_swiglu", M=M, N=N, K=K)
+    seg_off = np.array([0, M], np.int64)
+    out = dict(workload=wl, M=M, K=K, N=N, seg_off=seg_off)
+    out["x"] = make_x(dataclasses.replace(base, M=M, K=K), M)   # fc1's X recipe at this K
+    g = rng_for(base.base_seed + 200, T_W)
+    out["w"] = to_bf16_bits(g.standard_normal((N, K), dtype=np.float32) * np.float32(0.02))
+    out["bias"] = to_bf16_bits(rng_for(base.base_seed + 200, T_BIAS).standard_normal(N, dtype=np.float32)
+                               * np.float32(0.01))
+    out["shift"] = (rng_for(base.base_seed + 200, T_SHIFT).standard_normal((1, K), dtype=np.float32)
+                    * np.float32(0.1))
+    out["scale"] = (rng_for(base.base_seed + 200, T_SCALE).standard_normal((1, K), dtype=np.float32)
+                    * np.float32(0.1))
+    out["gate"] = out["resid"] = None
     return out
