@@ -134,13 +134,6 @@ __device__ __forceinline__ uint32_t swz64(uint32_t r, uint32_t j)
 
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
-{
-    const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-    const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-    return l | (h << 16);
-}
-
 // kSwiglu: SwiGLU epilogue (out [M][N/2]); kAmax: track max |out| into p.amax_out.
 // Compile-time, so that the plain epilogue carries neither.
 template <bool kSwiglu, bool kAmax>
@@ -372,6 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = e >> 2;              // column half of the 256-wide tile
         uint8_t* stg = smem + kEpiOff + e * kEpiWarpBytes;
         const float alpha = __fmul_rn(__ldg(p.a_gscale), __ldg(p.w_gscale));
+        const uint64_t alpha2 = f2(alpha, alpha);
         uint32_t acc_phase = 0, r_phase = 0;
         bool r_pending = false;
         float omax = 0.0f;  // max |out| over this lane's rows < M (before the bf16 rounding)
@@ -469,17 +463,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                             float o[8];
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const float g = bf16_round(
-                                    __fadd_rn(__fmul_rn(__uint_as_float(acc[cc][8 * j + i]), alpha), bg[i]));
-                                const float u = bf16_round(
-                                    __fadd_rn(__fmul_rn(__uint_as_float(acc[2 + cc][8 * j + i]), alpha), bu[i]));
-                                o[i] = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
-                                if (kAmax && row < p.M) omax = fmaxf(omax, fabsf(o[i]));
+                            for (int i = 0; i < 4; ++i) {
+                                // g, u exactly as the plain epilogue stores them (alpha*acc + b, one rounding, then bf16)
+                                const uint32_t gw = cvt_bf16x2(fma2(
+                                    f2(__uint_as_float(acc[cc][8 * j + 2 * i]), __uint_as_float(acc[cc][8 * j + 2 * i + 1])),
+                                    alpha2, f2(bg[2 * i], bg[2 * i + 1])));
+                                const uint32_t uw = cvt_bf16x2(fma2(
+                                    f2(__uint_as_float(acc[2 + cc][8 * j + 2 * i]),
+                                       __uint_as_float(acc[2 + cc][8 * j + 2 * i + 1])),
+                                    alpha2, f2(bu[2 * i], bu[2 * i + 1])));
+#pragma unroll
+                                for (int k = 0; k < 2; ++k) {
+                                    const float g = k ? __uint_as_float(gw & 0xFFFF0000u) : __uint_as_float(gw << 16);
+                                    const float u = k ? __uint_as_float(uw & 0xFFFF0000u) : __uint_as_float(uw << 16);
+                                    o[2 * i + k] = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+                                    if (kAmax && row < p.M) omax = fmaxf(omax, fabsf(o[2 * i + k]));
+                                }
                             }
                             *reinterpret_cast<uint4*>(buf + swz64(lane, j)) =
-                                make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
-                                           pack_bf16x2(o[6], o[7]));
+                                make_uint4(cvt_bf16x2(f2(o[0], o[1])), cvt_bf16x2(f2(o[2], o[3])),
+                                           cvt_bf16x2(f2(o[4], o[5])), cvt_bf16x2(f2(o[6], o[7])));
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
@@ -489,50 +492,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int n8 = nc0 + 32 * c + 8 * j;
-                        float b[8], g[8], r[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            b[i] = 0.0f;
-                            g[i] = 1.0f;
-                            r[i] = 0.0f;
-                        }
-                        if (n8 < p.N) {
-                            if (p.bias != nullptr) {
+                        // Lane pairs through the paired fp32 instructions (each lane
+                        // rounds like the scalar op): y = alpha*acc + b in one fma, then
+                        // out = g*y + R in one fma with the residual gate.
+                        uint64_t y2[4];
+                        {
+                            uint32_t bw[4] = {0u, 0u, 0u, 0u};
+                            if (n8 < p.N && p.bias != nullptr) {
                                 const uint4 bv = __ldg(reinterpret_cast<const uint4*>(p.bias + n8));
-                                const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+                                bw[0] = bv.x; bw[1] = bv.y; bw[2] = bv.z; bw[3] = bv.w;
+                            }
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    b[2 * i] = __uint_as_float(bw[i] << 16);
-                                    b[2 * i + 1] = __uint_as_float(bw[i] & 0xFFFF0000u);
-                                }
-                            }
-                            if (grow != nullptr) {
-                                const float4 g0 = __ldg(reinterpret_cast<const float4*>(grow + n8));
-                                const float4 g1 = __ldg(reinterpret_cast<const float4*>(grow + n8) + 1);
-                                g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
-                                g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
-                            }
+                            for (int i = 0; i < 4; ++i)
+                                y2[i] = fma2(f2(__uint_as_float(acc[c][8 * j + 2 * i]),
+                                                __uint_as_float(acc[c][8 * j + 2 * i + 1])),
+                                             alpha2, f2(__uint_as_float(bw[i] << 16), __uint_as_float(bw[i] & 0xFFFF0000u)));
                         }
                         uint4* slot = reinterpret_cast<uint4*>(buf + swz64(lane, j));
                         if (p.has_resid) {
                             const uint4 rv = *slot;
                             const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+                            float4 g0 = make_float4(1.0f, 1.0f, 1.0f, 1.0f), g1 = g0;
+                            if (grow != nullptr && n8 < p.N) {
+                                g0 = __ldg(reinterpret_cast<const float4*>(grow + n8));
+                                g1 = __ldg(reinterpret_cast<const float4*>(grow + n8) + 1);
+                            }
+                            const uint64_t g2[4] = {f2(g0.x, g0.y), f2(g0.z, g0.w), f2(g1.x, g1.y), f2(g1.z, g1.w)};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                y2[i] = fma2(g2[i], y2[i],
+                                             f2(__uint_as_float(rw[i] << 16), __uint_as_float(rw[i] & 0xFFFF0000u)));
+                        }
+                        if (kAmax && row < p.M && n8 < p.N) {
 #pragma unroll
                             for (int i = 0; i < 4; ++i) {
-                                r[2 * i] = __uint_as_float(rw[i] << 16);
-                                r[2 * i + 1] = __uint_as_float(rw[i] & 0xFFFF0000u);
+                                float lo, hi;
+                                unf2(y2[i], lo, hi);
+                                omax = fmaxf(omax, fmaxf(fabsf(lo), fabsf(hi)));
                             }
                         }
-                        float o[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float y = __fmul_rn(__uint_as_float(acc[c][8 * j + i]), alpha);
-                            const float v = __fadd_rn(y, b[i]);
-                            o[i] = (grow != nullptr) ? __fmaf_rn(g[i], v, r[i]) : __fadd_rn(v, r[i]);
-                            if (kAmax && row < p.M && n8 < p.N) omax = fmaxf(omax, fabsf(o[i]));
-                        }
-                        *slot = make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
-                                           pack_bf16x2(o[6], o[7]));
+                        *slot = make_uint4(cvt_bf16x2(y2[0]), cvt_bf16x2(y2[1]), cvt_bf16x2(y2[2]), cvt_bf16x2(y2[3]));
                     }
                     fence_proxy_async_smem();
                     __syncwarp();

@@ -48,35 +48,6 @@ struct QuantParams {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Two fp32 lanes in one 64-bit register for the paired fp32 instructions:
-// fma.rn.f32x2 / mul.rn.f32x2 round each lane exactly like the scalar
-// fma.rn.f32 / mul.rn.f32.
-__device__ __forceinline__ uint64_t f2(float lo, float hi)
-{
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-
-__device__ __forceinline__ void unf2(uint64_t v, float& lo, float& hi)
-{
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
-{
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
-{
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
 // Eight fp32 values -> eight E2M1 codes in one word, value 2i in bits 8i..8i+3
 // and value 2i+1 in bits 8i+4..8i+7 (RN, saturating to +-6, sign kept).
 __device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8])
