@@ -35,7 +35,7 @@ DEFAULT_CONFIG = "qkv"
 REFERENCE_BUDGET_S = 120.0  # CPU seconds the reference arm's timed steps aim for in total
 # DRAM bytes (read + write) per launch of nvfp4_gemm_kernel from one ncu capture
 # of the current kernel (profiles/nvfp4_gemm_qkv.md); None where not captured.
-NCU_GEMM_TRAFFIC = {"qkv": 30.299392e6 + 99.193088e6}
+NCU_GEMM_TRAFFIC = {"qkv": 30.247936e6 + 99.363584e6}
 
 
 def load_peaks():
