@@ -240,6 +240,88 @@ def time_mlp_chain(torch, A, steps: int, warmup: int, flush):
     return res
 
 
+def time_block_graph(torch, A, M: int, steps: int, flush):
+    """One transformer block's four projections at M tokens, issued eagerly and
+    as a replayed CUDA graph (audio_dit_gb300.graphs): QKV 3072 -> 9216 with the
+    prologue, attention output 3072 -> 3072 (two segments, gate, residual),
+    FC1 3072 -> 24576 with the SwiGLU producer and its amax, FC2 12288 -> 3072
+    on h with the derived scale. Device time per block, L2 flushed before each."""
+    from audio_dit_gb300.graphs import GraphBuckets
+    g = torch.Generator(device="cuda").manual_seed(1234)
+    rn = lambda *sh, std=1.0: torch.randn(*sh, generator=g, device="cuda") * std
+    K, NQ, NA, N1, N2 = 3072, 9216, 3072, 24576, 3072
+    H = N1 // 2
+    wq = {}
+    for name, (n, k) in {"qkv": (NQ, K), "att": (NA, K), "fc1": (N1, K), "fc2": (N2, H)}.items():
+        wq[name] = A.alloc_nvfp4(n, k)
+        wsw = A.alloc_workspace(n, 0, k, A.A_PREQUANT)
+        A.h3fp4_quantize_weight(rn(n, k, std=0.02).bfloat16(), *wq[name], wsw)
+    b = {n: rn(c, std=0.01).bfloat16() for n, c in [("qkv", NQ), ("att", NA), ("fc1", N1), ("fc2", N2)]}
+    sh, sc = rn(1, K, std=0.1), rn(1, K, std=0.1)
+    sh2, sc2 = rn(2, K, std=0.1), rn(2, K, std=0.1)
+    gate_a, gate_2 = torch.rand(2, NA, generator=g, device="cuda"), torch.rand(1, N2, generator=g, device="cuda")
+    x = {n: rn(M, K).bfloat16() for n in ("qkv", "att", "fc1")}
+    ra, r2 = rn(M, NA).bfloat16(), rn(M, N2).bfloat16()
+    out = {"qkv": torch.empty(M, NQ, dtype=torch.bfloat16, device="cuda"),
+           "att": torch.empty(M, NA, dtype=torch.bfloat16, device="cuda"),
+           "h": torch.empty(M, H, dtype=torch.bfloat16, device="cuda"),
+           "fc2": torch.empty(M, N2, dtype=torch.bfloat16, device="cuda")}
+    ws = {n: A.alloc_workspace(M, 0, k, 0) for n, k in [("qkv", K), ("att", K), ("fc1", K), ("fc2", H)]}
+    gs2 = torch.empty(1, dtype=torch.float32, device="cuda")
+    seg = [0, M - M // 32, M]
+
+    def issue(_key):
+        A.h3fp4_linear(x["qkv"], *wq["qkv"], out["qkv"], ws["qkv"], shift=sh, scale=sc, bias=b["qkv"])
+        A.h3fp4_linear(x["att"], *wq["att"], out["att"], ws["att"], shift=sh2, scale=sc2, gate=gate_a,
+                       resid=ra, bias=b["att"], seg_off=seg)
+        A.h3fp4_linear(x["fc1"], *wq["fc1"], out["h"], ws["fc1"], shift=sh, scale=sc, bias=b["fc1"],
+                       swiglu=True, out_amax=True)
+        A.h3fp4_gscale_from_amax(A.h3fp4_ws_out_amax(ws["fc1"]), gs2)
+        A.h3fp4_linear(out["h"], *wq["fc2"], out["fc2"], ws["fc2"], a_gscale=gs2, gscale_given=True,
+                       gate=gate_2, resid=r2, bias=b["fc2"])
+
+    graphs = GraphBuckets(issue)
+    graphs.capture(M)
+    s = torch.cuda.current_stream()
+    res = {}
+    for mode in ("eager", "graph"):
+        ts = []
+        for i in range(steps + 3):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            if mode == "eager":
+                issue(M)
+            else:
+                graphs.run(M)
+            e1.record(s)
+            torch.cuda.synchronize()
+            if i >= 3:
+                ts.append(e0.elapsed_time(e1))
+        res[mode + "_ms"] = round(float(np.median(ts)), 4)
+    # host time to issue one block (no synchronisation inside the measured region)
+    for mode in ("eager", "graph"):
+        hs = []
+        for i in range(steps + 3):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            if mode == "eager":
+                issue(M)
+            else:
+                graphs.run(M)
+            t1 = time.perf_counter()
+            if i >= 3:
+                hs.append((t1 - t0) * 1e6)
+        res[mode + "_host_issue_us"] = round(float(np.median(hs)), 1)
+    torch.cuda.synchronize()
+    for w in ws.values():
+        A.h3fp4_check(w)
+    flops = 2.0 * M * (K * NQ + K * NA + K * N1 + H * N2)
+    res["graph_tflops"] = round(flops / (res["graph_ms"] * 1e-3) / 1e12, 1)
+    res["launches_per_block"] = "12 kernels + 1 memset"
+    return res
+
+
 def time_device_steps(torch, A, prob: Problem, steps: int, warmup: int, flush, given_scale: bool = False):
     """Per-step CUDA events on the launching stream: [quant | gemm], L2 flushed
     between steps. With given_scale the quantisation is the pack pass alone
@@ -479,6 +561,12 @@ def run_gpu(args):
             extra["mlp_swiglu"] = time_mlp_chain(torch, A, max(3, min(50, args.steps // 40)), 3, flush)
         except Exception as e:
             extra["mlp_swiglu"] = {"error": repr(e)[:200]}
+        for bm in (1024, 8192):
+            try:
+                extra[f"block_graph_m{bm}"] = time_block_graph(torch, A, bm, max(3, min(30, args.steps // 60)), flush)
+                torch.cuda.empty_cache()
+            except Exception as e:
+                extra[f"block_graph_m{bm}"] = {"error": repr(e)[:200]}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
