@@ -61,6 +61,7 @@ def _check_swiglu(orc, y, h, rows=None):
     d = _ulp_diff(hh, ref)
     assert d.max() <= 1, f"{int((d > 1).sum())} SwiGLU outputs more than one bf16 step off"
     exact = float((d == 0).mean())
+    print(f"SwiGLU bit-identical fraction {exact:.6f} over {d.size} outputs")
     assert exact >= 0.999, f"only {exact:.5f} of SwiGLU outputs bit-identical"
     return exact
 
