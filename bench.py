@@ -216,8 +216,20 @@ def time_mlp_chain(torch, A, steps: int, warmup: int, flush):
     for _ in range(warmup):
         flush(); fc1(); fc2(True); fc2(False)
     torch.cuda.synchronize()
+    # FC1's GEMM alone (X quantised beforehand) for its tensor roofline
+    xq = A.alloc_nvfp4(M, K1)
+    A.h3fp4_quantize_act(x, *xq, ws1, shift=sh, scale=sc)
+    def fc1_gemm():
+        A.h3fp4_linear(xq[0], *wq1, h, ws1, a_sf=xq[1], a_gscale=xq[2], bias=b1, swiglu=True, out_amax=True)
+    fc1_gemm()
+    t1g = []
     t1, t2, t2b = [], [], []
     for _ in range(steps):
+        flush()
+        eg = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        eg[0].record(s); fc1_gemm(); eg[1].record(s)
+        torch.cuda.synchronize()
+        t1g.append(eg[0].elapsed_time(eg[1]))
         flush()
         e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
         e[0].record(s); fc1(); e[1].record(s); fc2(True); e[2].record(s)
@@ -230,8 +242,11 @@ def time_mlp_chain(torch, A, steps: int, warmup: int, flush):
     A.h3fp4_check(ws2)
     flops = 2.0 * M * K1 * N1 + 2.0 * M * K2 * N2
     step = float(np.mean(t1) + np.mean(t2))
+    fc1_gemm_ms = float(np.mean(t1g))
+    fc1_gemm_tflops = 2.0 * M * K1 * N1 / (fc1_gemm_ms * 1e-3) / 1e12
     res = {"tflops": round(flops / (step * 1e-3) / 1e12, 1), "ms_per_step": round(step, 4),
            "fc1_swiglu_ms": round(float(np.mean(t1)), 4),
+           "fc1_swiglu_gemm_ms": round(fc1_gemm_ms, 4), "fc1_swiglu_gemm_tflops": round(fc1_gemm_tflops, 1),
            "fc2_producer_amax_ms": round(float(np.mean(t2)), 4),
            "fc2_two_pass_ms": round(float(np.mean(t2b)), 4),
            "shape": f"X [{M},{K1}] -> FC1 [{N1},{K1}] + SwiGLU -> h [{M},{N1 // 2}] -> FC2 [{N2},{K2}] + gate/resid"}
@@ -559,6 +574,8 @@ def run_gpu(args):
                 extra[name] = {"error": repr(e)[:200]}
         try:
             extra["mlp_swiglu"] = time_mlp_chain(torch, A, max(3, min(50, args.steps // 40)), 3, flush)
+            extra["mlp_swiglu"]["fc1_swiglu_gemm_frac_fp4_peak"] = round(
+                extra["mlp_swiglu"]["fc1_swiglu_gemm_tflops"] / fp4_peak, 4)
         except Exception as e:
             extra["mlp_swiglu"] = {"error": repr(e)[:200]}
         for bm in (1024, 8192):

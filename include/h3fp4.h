@@ -60,6 +60,11 @@
  *   - The GEMM runs as clusters of two CTAs (512 threads, ~228 KB of shared
  *     memory and all 512 TMEM columns each), one CTA per SM, over every SM
  *     pair that can be co-resident.
+ *   - Calls issue only kernel launches and (with H3FP4_EPI_AMAX) one memset
+ *     on `stream`, so a fixed sequence of calls can be captured into a CUDA
+ *     graph.  Make one eager call per device before the first capture: it
+ *     performs the library's one-time per-device setup (kernel attributes,
+ *     occupancy queries).
  */
 #ifndef H3FP4_H
 #define H3FP4_H
