@@ -6,6 +6,11 @@
 //               ("H3 Runtime Current State", "Owned Performance Kernels":
 //               alpha-before-BF16 epilogue; "Implemented And Validated": fused
 //               residual gates).
+// or, for FC1 feeding FC2 (kSwiglu; the same section's exact SwiGLU-to-FC2
+// producer fusion, which keeps the two BF16 boundaries):
+//   out[m][128 t + i] = bf16( silu(g) * u ),  g, u = bf16(alpha * acc + b) of the
+//               gate column 256 t + i and the up column 256 t + 128 + i,
+// and optionally (kAmax) max |out| over the call, for FC2's one-pass quantisation.
 //
 // CTA pairs.  The kernel runs as clusters of two CTAs on two SMs; a pair owns
 // a 256 x 256 output tile.  CTA r of the pair loads the 128 rows
@@ -41,10 +46,14 @@
 //               tensor pipe (about 75 cycles per extra wait per 513-cycle stage).
 //   warps 8-15  epilogue (both): tcgen05.ld the CTA's 128 x 256 fp32
 //               accumulator (each warp 32 rows x 128 columns), release it to
-//               the leader, then alpha/bias/gate/residual in fp32 and bf16
-//               stores in two passes of two 32x32 chunks, each through two
+//               the leader, then alpha/bias/gate/residual on paired fp32
+//               instructions (fma.rn.f32x2, cvt.rn.bf16x2.f32: the epilogue
+//               shares issue slots with the producer, MMA and scale warps) and
+//               bf16 stores in two passes of two 32x32 chunks, each through two
 //               64-byte-swizzled staging buffers and TMA stores; a pass's
 //               residual chunks are TMA-loaded into those buffers first.
+//               SwiGLU: gate and up columns of 32 rows x 64 hidden units per
+//               warp, one pass.
 // Each kernel launch may start while the previous kernel of the stream drains
 // (programmatic dependent launch); it reads no input before griddepcontrol.wait.
 // Registers per thread (setmaxnreg): warpgroup 0: 40, scale warps: 96,
