@@ -227,11 +227,18 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(QuantParams p)
             if (kMod && r + u >= mc.seg_end) load_mod(p, segment_of(p.seg, r + u), cb, mc);
             float f[16];
             unpack16(v[u], f);
-            modulate16<kMod>(f, mc);
+            if (kMod) {
+                // The modulated values before their bf16 rounding: rounding to
+                // nearest is monotone and odd, so the largest |bf16(m)| is the
+                // bf16 rounding of the largest |m|, applied once below.
+#pragma unroll
+                for (int j = 0; j < 8; ++j) unf2(fma2(f2(f[2 * j], f[2 * j + 1]), mc.onep[j], mc.sh[j]), f[2 * j], f[2 * j + 1]);
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) mx = fmaxf(mx, fabsf(f[j]));
         }
     }
+    if (kMod) mx = __bfloat162float(__float2bfloat16_rn(mx));
     const float m = block_reduce_max(mx, red);
     if (threadIdx.x == 0) p.partials[blockIdx.y * gridDim.x + blockIdx.x] = m;
 }
