@@ -117,3 +117,14 @@ def test_swiglu_chain_into_fc2_quantisation(orc):
     A.h3fp4_linear(h, *wq, out_amax, ws2)
     A.h3fp4_check(ws2)
     assert torch.equal(out_given.view(torch.int16), out_amax.view(torch.int16))
+
+
+def test_out_amax_with_gate_residual_and_segments():
+    """The output amax of the gated epilogue (two segments, residual) is exactly
+    max |out| of the stored bf16 output, including a ragged last tile."""
+    import audio_dit_gb300 as A
+    d = W.make_inputs("attn_out", M=333)
+    case = LinearCase(d)
+    out = case.run(out_amax=True)
+    torch.cuda.synchronize()
+    _check_amax(out, A.h3fp4_ws_out_amax(case.ws).clone())
