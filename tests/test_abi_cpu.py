@@ -73,6 +73,19 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.h3fp4_status_string(5) == b"device wait timed out"
 
 
+def test_swiglu_and_amax_flags_pass_host_validation(lib):
+    # Valid shapes and flags get past every host check; without a GPU the call
+    # then stops at the device check (CUDA error or unsupported device).
+    vp = C.c_void_p
+    dummy = vp(4096)
+    for flags in (64, 128, 64 | 128, 64 | 128 | 2 | 1):
+        shift = dummy if flags & 1 else None
+        out = vp(8192)   # must not alias x
+        r = lib.h3fp4_linear(dummy, None, None, 16, 512, 64, dummy, dummy, dummy, shift, shift, None, None, 1,
+                             dummy if flags & 2 else None, None, out, flags, dummy, None)
+        assert r in (4, 6), (flags, r)
+
+
 def test_ws_out_amax_address(lib):
     import audio_dit_gb300 as A
     lib.h3fp4_ws_out_amax.restype = C.c_void_p
