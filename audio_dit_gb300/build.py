@@ -62,7 +62,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
         list(ex.map(run, jobs))
     if force or jobs or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcuda" if False else "-lcudart_static", "-ldl", "-lrt",
+        run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-ldl", "-lrt",
              "-lpthread"])
         os.replace(tmp, LIB)
     return LIB

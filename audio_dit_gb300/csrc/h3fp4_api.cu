@@ -18,9 +18,13 @@ std::once_flag g_dev_once[kMaxDevices];
 int g_dev_ok[kMaxDevices];
 int g_dev_sms[kMaxDevices];
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+h3fp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? H3FP4_OK : H3FP4_ERR_CUDA; }
+
+}  // namespace
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 h3fp4_status check_device()
 {
@@ -64,10 +68,6 @@ h3fp4_status check_shape(int64_t rows, int64_t K)
     if (rows * (K / 8) > (int64_t)INT32_MAX * 8) return H3FP4_ERR_SHAPE;
     return H3FP4_OK;
 }
-
-h3fp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? H3FP4_OK : H3FP4_ERR_CUDA; }
-
-}  // namespace
 
 cudaError_t ensure_dynamic_smem(const void* func, int bytes)
 {

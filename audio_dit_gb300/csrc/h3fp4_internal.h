@@ -75,6 +75,15 @@ cudaError_t launch_gscale_from_amax(const float* amax, float* gscale, cudaStream
 
 int sm_count_current_device();
 
+// Host-side validation shared by every entry point (defined in h3fp4_api.cu).
+bool aligned16(const void* p);
+// H3FP4_OK on an sm_103 current device, else ERR_UNSUPPORTED_DEVICE / ERR_CUDA.
+h3fp4_status check_device();
+// Copies and validates the host segment table (nseg <= 0 is read as 1).
+h3fp4_status make_segments(const int64_t* seg_off, int nseg, int64_t rows, Segments* out);
+// rows >= 1, K a positive multiple of 64 within the amax-partials budget.
+h3fp4_status check_shape(int64_t rows, int64_t K);
+
 // Sets cudaFuncAttributeMaxDynamicSharedMemorySize of `func` on the current
 // device the first time it is asked for that (function, device) pair; the
 // attribute belongs to each device's context.

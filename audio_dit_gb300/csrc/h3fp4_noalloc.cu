@@ -20,7 +20,6 @@
 // clearing, but calls that can overlap on the GPU (different streams, or
 // several host threads) race on the array and must be serialised by the caller.
 #include <cstdint>
-#include <cstring>
 #include <mutex>
 
 #include "h3fp4_internal.h"
@@ -30,14 +29,14 @@ namespace {
 
 constexpr int kNoAllocPartials = kMaxPartials;  // 4096 fp32 partial maxima
 constexpr int kNoAllocMaxDevices = 64;
+static_assert(kNoAllocPartials >= kMaxPartials, "the amax pass may write kMaxPartials partials");
 
 static __device__ __align__(256) float g_noalloc_partials[kNoAllocPartials];
 
-std::once_flag g_addr_once[kNoAllocMaxDevices];
+// Device address of the array per device; a failed look-up is not cached, so
+// a later call retries it.
+std::mutex g_addr_mu;
 float* g_addr[kNoAllocMaxDevices];
-cudaError_t g_addr_err[kNoAllocMaxDevices];
-
-bool is_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 }  // namespace h3fp4
@@ -48,51 +47,41 @@ extern "C" h3fp4_status h3fp4_quantize_act_noalloc(const void* x_bf16, int64_t M
                                                    const float* scale, const int64_t* seg_off, int nseg, void* codes,
                                                    void* sf, float* gscale, int flags, cudaStream_t stream)
 {
-    // Shapes: every 1024-column slab of a row needs at least one partial, so K
-    // is capped at kNoAllocPartials * 1024 columns; rows are unbounded by the
-    // scratch (the grid is sized to the partial count).
-    if (M < 1 || K < 64 || K % 64 != 0 || M > (int64_t)INT32_MAX) return H3FP4_ERR_SHAPE;
+    // Validation is shared with h3fp4_quantize_act, so both entries accept and
+    // reject the same arguments.  check_shape caps K at kMaxPartials * 1024
+    // columns: every 1024-column slab of a row needs one partial, and the grid
+    // is sized to at most kNoAllocPartials partials, so rows are unbounded by
+    // the scratch.
+    h3fp4_status st = check_shape(M, K);
+    if (st != H3FP4_OK) return st;
     if (K > (int64_t)kNoAllocPartials * 1024) return H3FP4_ERR_SHAPE;
-    if (M * (K / 8) > (int64_t)INT32_MAX * 8) return H3FP4_ERR_SHAPE;
     if (!x_bf16 || !codes || !sf || !gscale) return H3FP4_ERR_INVALID;
     if (flags & ~(H3FP4_PROLOGUE_MOD | H3FP4_GSCALE_GIVEN)) return H3FP4_ERR_INVALID;
     const bool mod = (flags & H3FP4_PROLOGUE_MOD) != 0;
     if (mod && (!shift || !scale)) return H3FP4_ERR_INVALID;
-    if (!is_aligned16(x_bf16) || !is_aligned16(codes) || !is_aligned16(sf) ||
-        (reinterpret_cast<uintptr_t>(gscale) & 3u) || (mod && (!is_aligned16(shift) || !is_aligned16(scale))))
+    if (!aligned16(x_bf16) || !aligned16(codes) || !aligned16(sf) || (reinterpret_cast<uintptr_t>(gscale) & 3u) ||
+        (mod && (!aligned16(shift) || !aligned16(scale))))
         return H3FP4_ERR_ALIGN;
-
     QuantJob job{};
-    std::memset(&job.seg, 0, sizeof(job.seg));
-    if (seg_off == nullptr) {
-        if (nseg > 1) return H3FP4_ERR_INVALID;
-        job.seg.nseg = 1;
-        job.seg.off[1] = M;
-    } else {
-        if (nseg < 1 || nseg > H3FP4_MAX_SEGMENTS) return H3FP4_ERR_SHAPE;
-        if (seg_off[0] != 0 || seg_off[nseg] != M) return H3FP4_ERR_INVALID;
-        for (int i = 0; i < nseg; ++i)
-            if (seg_off[i + 1] < seg_off[i]) return H3FP4_ERR_INVALID;
-        job.seg.nseg = nseg;
-        for (int i = 0; i <= nseg; ++i) job.seg.off[i] = seg_off[i];
-    }
+    st = make_segments(seg_off, nseg <= 0 ? 1 : nseg, M, &job.seg);
+    if (st != H3FP4_OK) return st;
+    if ((st = check_device()) != H3FP4_OK) return st;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return H3FP4_ERR_CUDA;
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-        return H3FP4_ERR_CUDA;
-    if (major != 10 || minor != 3) return H3FP4_ERR_UNSUPPORTED_DEVICE;
-
     // One-time set-up per device, with that device current: the device address
-    // of the scratch array.
-    std::call_once(g_addr_once[dev], [dev] {
-        void* p = nullptr;
-        g_addr_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_partials);
-        g_addr[dev] = static_cast<float*>(p);
-    });
-    if (g_addr_err[dev] != cudaSuccess || g_addr[dev] == nullptr) return H3FP4_ERR_CUDA;
+    // of the scratch array (cached for the life of the process; see the header
+    // for cudaDeviceReset).
+    float* partials = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_addr_mu);
+        if (g_addr[dev] == nullptr) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || p == nullptr) return H3FP4_ERR_CUDA;
+            g_addr[dev] = static_cast<float*>(p);
+        }
+        partials = g_addr[dev];
+    }
 
     job.x = x_bf16;
     job.rows = M;
@@ -103,6 +92,6 @@ extern "C" h3fp4_status h3fp4_quantize_act_noalloc(const void* x_bf16, int64_t M
     job.sf = static_cast<uint8_t*>(sf);
     job.gscale = gscale;
     job.gscale_given = (flags & H3FP4_GSCALE_GIVEN) != 0;
-    job.partials = g_addr[dev];
+    job.partials = partials;
     return launch_quantize(job, stream) == cudaSuccess ? H3FP4_OK : H3FP4_ERR_CUDA;
 }

@@ -99,25 +99,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
         : "memory");
 }
 
-__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t c0,
-                                                 int32_t c1, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "l"(policy)
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
-
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t c0, int32_t c1)
 {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
@@ -139,20 +120,6 @@ __device__ __forceinline__ void fence_proxy_async_smem()
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_last()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-__device__ __forceinline__ uint64_t l2_policy_evict_first()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
 }
 
 // ------------------------------------------------------------------ tcgen05
@@ -196,13 +163,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar)
                  : "memory");
 }
 
-// Copy a 32-row x 16-byte smem matrix into TMEM columns [taddr, taddr+4),
-// replicated into all four 32-lane groups.
-__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 __device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // 32 lanes x 32 consecutive fp32 columns: thread i receives lane (base + i).
@@ -238,32 +198,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
 
 // ------------------------------------------------------------------ narrow converts
 
-// Two fp32 -> two E2M1 codes in one byte: `lo` in bits 0-3, `hi` in bits 4-7.
-__device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi)
-{
-    uint16_t r;
-    asm("{\n\t.reg .b8 t;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\t"
-        "mov.b16 %0, {t, 0};\n\t}"
-        : "=h"(r)
-        : "f"(lo), "f"(hi));
-    return r;
-}
-
 // fp32 -> E4M3 code (round to nearest even, saturating to 448).
 __device__ __forceinline__ uint32_t cvt_e4m3(float x)
 {
     uint16_t r;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(r) : "f"(x), "f"(0.0f));
     return r & 0xFFu;
-}
-
-// E4M3 code (sign bit clear) -> fp32, exactly, from the format definition:
-// exponent field e, mantissa m: e > 0 -> 2^(e-7) * (1 + m/8); e == 0 -> m * 2^-9.
-__device__ __forceinline__ float e4m3_to_f32(uint32_t code)
-{
-    const uint32_t e = (code >> 3) & 15u, m = code & 7u;
-    return e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;
 }
 
 // Streaming 16-byte global load that does not allocate in L1.
@@ -290,40 +230,6 @@ __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-
-// TMA tile load delivered to the same smem offset (and mbarrier offset) of every
-// CTA in `mask`.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, uint64_t* bar, int32_t c0,
-                                               int32_t c1, uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(map), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_load_mc(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                             uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "h"(mask)
-        : "memory");
-}
-
-// tcgen05.commit arriving on the mbarrier at the same offset in every CTA of `mask`.
-__device__ __forceinline__ void tc_commit_mc(uint64_t* bar, uint16_t mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -407,14 +313,6 @@ __device__ __forceinline__ void tmem_relinquish_pair()
 __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
 {
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-// Issued by one thread of the leader CTA: each CTA of the pair copies the
-// 32x16-byte tile at this shared-memory offset of ITS OWN shared memory into
-// its own TMEM columns [taddr, taddr+4), replicated into all four lane quarters.
-__device__ __forceinline__ void tc_cp_pair_32x128b_warpx4(uint32_t taddr, uint64_t sdesc)
-{
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Paired block-scaled MMA (M = 256 over the two CTAs): each CTA supplies 128 rows

@@ -34,7 +34,7 @@ FP4_OVER_BF16 = 6.0   # nominal dense fp4 / bf16 tensor ratio (13.5 / 2.25 PFLOP
 DEFAULT_CONFIG = "qkv"
 REFERENCE_BUDGET_S = 120.0  # CPU seconds the reference arm's timed steps aim for in total
 # DRAM bytes (read + write) per launch of nvfp4_gemm_kernel from one ncu capture
-# of the current kernel (profiles/nvfp4_gemm_qkv.md); None where not captured.
+# of the current kernel per workload; None where not captured.
 NCU_GEMM_TRAFFIC = {"qkv": 30.247936e6 + 99.363584e6}
 
 

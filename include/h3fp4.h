@@ -190,9 +190,12 @@ H3FP4_API h3fp4_status h3fp4_linear(const void* x, const void* a_sf, const float
  *   library (4096 fp32 = 16 KiB), held by every GPU that loads the library
  *   until the process exits.  The first call on a device looks up the array's
  *   device address (cudaGetSymbolAddress) with that device current; make that
- *   first call before any stream capture.  All calls share the array: calls
- *   that can overlap on the GPU (several streams or host threads) race on it
- *   and must be serialised by the caller.
+ *   first call before any stream capture.  The address is cached per device
+ *   for the life of the process (a failed look-up is retried by the next
+ *   call); cudaDeviceReset reloads the library's device code, so a process
+ *   that resets a device must not call this entry point on it afterwards.
+ *   All calls share the array: calls that can overlap on the GPU (several
+ *   streams or host threads) race on it and must be serialised by the caller.
  *   Limit: K <= 4096 * 1024 columns (one partial per 1024-column slab at
  *   least); larger K returns H3FP4_ERR_SHAPE.
  *   Other arguments, results and errors as in h3fp4_quantize_act. */

@@ -73,9 +73,39 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.h3fp4_status_string(5) == b"device wait timed out"
 
 
+def test_noalloc_entry_validates_like_the_workspace_entry(lib):
+    # Both quantiser entries share their host validation: the same bad
+    # arguments give the same status, decided before any launch.
+    vp = C.c_void_p
+    d = vp(4096)
+    seg_bad = (C.c_int64 * 3)(0, 5, 17)
+    seg_ok = (C.c_int64 * 3)(0, 5, 16)
+    cases = [
+        (d, 16, 100, None, None, None, 1, d, d, d, 0),            # K % 64
+        (d, 0, 64, None, None, None, 1, d, d, d, 0),              # no rows
+        (d, 16, 64 * 4096 * 1024 // 64 * 64 + 64, None, None, None, 1, d, d, d, 0),  # K over the cap
+        (None, 16, 64, None, None, None, 1, d, d, d, 0),          # null input
+        (vp(4097), 16, 64, None, None, None, 1, d, d, d, 0),      # misaligned input
+        (d, 16, 64, None, None, None, 1, d, d, d, 1),             # prologue without vectors
+        (d, 16, 64, None, None, None, 1, d, d, d, 1 << 9),        # unknown flag
+        (d, 16, 64, None, None, C.cast(seg_bad, vp), 2, d, d, d, 0),   # table does not end at M
+        (d, 16, 64, None, None, C.cast(seg_ok, vp), 0, d, d, d, 0),    # nseg <= 0 read as 1: ends at 5, not M
+        (d, 16, 64, None, None, C.cast(seg_ok, vp), 99, d, d, d, 0),   # too many segments
+    ]
+    for c in cases:
+        a = lib.h3fp4_quantize_act(*c, d, None)
+        b = lib.h3fp4_quantize_act_noalloc(*c, None)
+        assert a == b and a in (1, 2, 3), (c[1:3], c[-1], a, b)
+
+
 def test_swiglu_and_amax_flags_pass_host_validation(lib):
     # Valid shapes and flags get past every host check; without a GPU the call
-    # then stops at the device check (CUDA error or unsupported device).
+    # then stops at the device check (CUDA error or unsupported device).  The
+    # pointers are fake, so with a CUDA device visible the call would launch
+    # on them: the test runs only where no device exists.
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("fake device pointers: host-validation check runs only without a CUDA device")
     vp = C.c_void_p
     dummy = vp(4096)
     for flags in (64, 128, 64 | 128, 64 | 128 | 2 | 1):
