@@ -81,6 +81,7 @@ def lib():
                 "orc_num_threads": (C.c_int, []),
                 "orc_swiglu_bf16": (C.c_uint16, [C.c_uint16, C.c_uint16]),
                 "orc_swiglu_rows": (None, [vp, i64, i64, vp]),
+                "orc_silu_mul_f64": (None, [vp, vp, i64, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -263,6 +264,16 @@ def swiglu_rows(y_bf16) -> np.ndarray:
     h = np.empty((rows, n2 // 2), np.uint16)
     lib().orc_swiglu_rows(_p(y), rows, n2 // 2, _p(h))
     return h
+
+
+def silu_mul_f64(g, u) -> np.ndarray:
+    """silu(g) * u in float64 for float64 arrays g, u (no bf16 rounding)."""
+    g = _c(g, np.float64).ravel()
+    u = _c(u, np.float64).ravel()
+    assert g.shape == u.shape
+    out = np.empty(g.size, np.float64)
+    lib().orc_silu_mul_f64(_p(g), _p(u), g.size, _p(out))
+    return out
 
 
 def gemm_f64(a: np.ndarray, w: np.ndarray) -> np.ndarray:

@@ -351,6 +351,21 @@ ORC_API uint16_t orc_swiglu_bf16(uint16_t g, uint16_t u)
     return bf16_round(silu * ud, 0);
 }
 
+/* silu(g) * u for real-valued g, u, in float64 with no rounding to bf16: the
+ * value the SwiGLU producer rounds (R8), here taken at the unrounded float64
+ * FC1 outputs, so that an end-to-end bound can be stated around it.  Small |g|
+ * uses silu(g) = g/2 + g^2/4 + O(g^4), where g / (1 + e^-g) would lose the
+ * g^2 term to rounding. */
+ORC_API void orc_silu_mul_f64(const double* g, const double* u, int64_t n, double* out)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        double gd = g[i];
+        double silu = fabs(gd) < 0x1p-20 ? 0.5 * gd + 0.25 * gd * gd : gd / (1.0 + exp(-gd));
+        out[i] = silu * u[i];
+    }
+}
+
 /* Elementwise over an FC1 output in the SwiGLU row layout: y [rows][2*H] holds,
  * for every group t of 128 hidden units, the 128 gate columns [256 t, 256 t + 128)
  * followed by the matching 128 up columns; h [rows][H]. */

@@ -16,8 +16,8 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
-from _gpu_helpers import (LinearCase, assert_quant_equal, check_outputs, host_u16,  # noqa: E402
-                          oracle_operands, sample_points)
+from _gpu_helpers import (Guarded, LinearCase, assert_quant_equal, check_outputs, host_u16,  # noqa: E402
+                          oracle_operands, sample_points, tile_points)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -46,12 +46,17 @@ def test_reduced_rows_all_outputs(orc, name, M):
 
 
 @pytest.mark.parametrize("name", ["qkv", "fc1", "fc2", "attn_out"])
-def test_full_size_sampled(orc, name):
+def test_full_size_every_tile(orc, name):
+    """Full size, as the bench runs it: every epilogue warp of every 256 x 256
+    pair tile (both CTAs, all four lane quarters, both column halves; every
+    round of the persistent loop and the partial last wave) contributes one
+    point, plus random points and the segment edges."""
     d = W.make_inputs(name)
     case = LinearCase(d)
     out = host_u16(case.run())
     a, w = oracle_operands(orc, d)
-    pts = sample_points(d["M"], d["N"], 1500, seed=sum(name.encode()), seg_off=d["seg_off"])
+    pts = np.concatenate([tile_points(d["M"], d["N"], seed=sum(name.encode())),
+                          sample_points(d["M"], d["N"], 500, seed=sum(name.encode()), seg_off=d["seg_off"])])
     ref, bound = orc.linear_points(a, w, d["M"], d["N"], d["K"], pts, bias=d["bias"], gate=d["gate"],
                                    resid=d["resid"], seg_off=d["seg_off"])
     check_outputs(out[pts[:, 0], pts[:, 1]], ref, bound, f"{name} full size")
@@ -116,7 +121,7 @@ def test_m_sweep_sampled(orc, M):
     case = LinearCase(d)
     out = host_u16(case.run())
     a, w = oracle_operands(orc, d)
-    pts = sample_points(M, d["N"], 600, seed=M)
+    pts = np.concatenate([tile_points(M, d["N"], seed=M), sample_points(M, d["N"], 300, seed=M)])
     ref, bound = orc.linear_points(a, w, M, d["N"], d["K"], pts, bias=d["bias"], gate=d["gate"],
                                    resid=d["resid"], seg_off=d["seg_off"])
     check_outputs(out[pts[:, 0], pts[:, 1]], ref, bound, f"sweep M={M}")
@@ -128,3 +133,13 @@ def test_repeat_is_deterministic():
     o1 = case.run().clone()
     o2 = case.run().clone()
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+def test_guard_regions_detect_a_stray_write():
+    """The canary check used by every linear/quantise test fires on a write
+    just past a buffer (made here by torch, not by the library)."""
+    g = Guarded((3, 100), torch.bfloat16)
+    g.check("clean")
+    g.raw[g.raw.numel() - 1] = 0
+    with pytest.raises(AssertionError):
+        g.check("planted")

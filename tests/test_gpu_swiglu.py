@@ -22,7 +22,8 @@ torch = pytest.importorskip("torch")
 if not torch.cuda.is_available():
     pytest.skip("needs a CUDA device", allow_module_level=True)
 
-from _gpu_helpers import LinearCase, assert_quant_equal, gpu_quantize, host_u16  # noqa: E402
+from _gpu_helpers import (Guarded, LinearCase, assert_quant_equal, gpu_quantize, host_u16,  # noqa: E402
+                          oracle_operands)
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -45,10 +46,12 @@ def _run_pair(d, rows=None):
     case = LinearCase(d)
     y = case.run(out_amax=True).clone()
     amax_plain = A.h3fp4_ws_out_amax(case.ws).clone()
-    h = torch.empty((d["M"], d["N"] // 2), dtype=torch.bfloat16, device="cuda")
+    gh = Guarded((d["M"], d["N"] // 2), torch.bfloat16)
+    h = gh.t
     A.h3fp4_linear(case.x, *case.wq, h, case.ws, shift=case.shift, scale=case.scale, bias=case.bias,
                    swiglu=True, out_amax=True)
     A.h3fp4_check(case.ws)
+    case.check_guards([gh])
     amax_h = A.h3fp4_ws_out_amax(case.ws).clone()
     torch.cuda.synchronize()
     return case, y, h, amax_plain, amax_h
@@ -81,9 +84,60 @@ def test_swiglu_matches_plain_epilogue(orc, M, N, K):
     _check_amax(h, amax_h)
 
 
+# Largest |silu'(g)| over all real g (about 1.0998, near g = 2.4).
+SILU_LIPSCHITZ = 1.1
+
+
+def swiglu_end_to_end_bound(silu_yg, bg, yu, bu, h_true):
+    """Tolerance for h = bf16(silu(g) * u) computed from GPU FC1 values g, u
+    that lie within bg, bu of the oracle's float64 FC1 outputs yg, yu (the
+    linear's own bound, bf16 rounding of g and u included):
+      |silu(g) u - silu(yg) yu| <= (|silu(yg)| + L bg) bu + L bg |yu|,  L = max|silu'|,
+    then h's own rounding to bf16 (half a step, <= 2^-8 relative) and the fp32
+    evaluation of silu (a few fp32 ulps, < 2^-20 relative) of the value reached."""
+    first = (np.abs(silu_yg) + SILU_LIPSCHITZ * bg) * bu + SILU_LIPSCHITZ * bg * np.abs(yu)
+    return first + (2.0 ** -8 + 2.0 ** -20) * (np.abs(h_true) + first)
+
+
+def test_swiglu_full_size_end_to_end(orc):
+    """FC1 with the SwiGLU producer at its full size (X [32768, 3072] with the
+    prologue, W [24576, 3072]) -> h [32768, 12288], against the oracle end to
+    end: the float64 oracle FC1 outputs of the gate and up columns, silu(g) * u
+    of those in float64, and the derived bound above.  Rows: one per 256-row
+    pair tile of M (alternating the CTA of the pair and the lane quarter) plus
+    the edges, every h column of each."""
+    d = W.swiglu_fc1_inputs(32768)
+    M, N = d["M"], d["N"]
+    _, y, h, _, amax_h = _run_pair(d)
+    _check_amax(h, amax_h)
+    rng = np.random.default_rng(11)
+    t = np.arange((M + 255) // 256)
+    rows = np.unique(np.concatenate([256 * t + 128 * (t % 2) + 32 * ((t // 2) % 4) + rng.integers(0, 32, t.size),
+                                     [0, 127, 128, 255, 256, M - 1]]))
+    rows = rows[rows < M]
+    H = N // 2
+    j = np.arange(H)
+    gcol = 256 * (j // 128) + j % 128
+    rr = np.repeat(rows, H)
+    pts_g = np.stack([rr, np.tile(gcol, rows.size)], axis=1).astype(np.int64)
+    pts_u = pts_g + np.array([0, 128], np.int64)
+    a, w = oracle_operands(orc, d)
+    yg, bg = orc.linear_points(a, w, M, N, d["K"], pts_g, bias=d["bias"])
+    yu, bu = orc.linear_points(a, w, M, N, d["K"], pts_u, bias=d["bias"])
+    h_true = orc.silu_mul_f64(yg, yu)
+    bound = swiglu_end_to_end_bound(orc.silu_mul_f64(yg, np.ones_like(yg)), bg, yu, bu, h_true)
+    got = W.bf16_bits_to_f32(host_u16(h)[rows].ravel()).astype(np.float64)
+    err = np.abs(got - h_true)
+    ratio = float(np.max(err / np.maximum(bound, 1e-300)))
+    print(f"SwiGLU end to end: {got.size} outputs over {rows.size} rows, max err/bound {ratio:.3f}")
+    assert (err <= bound).all(), (f"{int((err > bound).sum())} h outside the end-to-end bound; "
+                                  f"max err/bound {ratio:.3g}")
+
+
 def test_swiglu_full_size_sampled_rows(orc):
-    """FC1 at its full size (X [32768, 3072], W [24576, 3072]) -> h [32768, 12288]:
-    sampled rows (tile and pair edges included) against the oracle, the amax exactly."""
+    """FC1 at its full size -> h: sampled rows (tile and pair edges included)
+    against the oracle's SwiGLU of the GPU's own plain FC1 output (one bf16
+    step, 99.9 % bit-identical)."""
     d = W.swiglu_fc1_inputs(32768)
     _, y, h, _, amax_h = _run_pair(d)
     rng = np.random.default_rng(11)

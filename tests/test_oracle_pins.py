@@ -493,3 +493,29 @@ def test_swiglu_rows_pairing(orc):
         for j in range(256):
             t, i = divmod(j, 128)
             assert h[r, j] == orc.swiglu_bf16(int(y[r, 256 * t + i]), int(y[r, 256 * t + 128 + i]))
+
+
+def _exact_silu_mul(g: float, u: float, prec=60):
+    """silu(g) * u for float64 g, u with 60-digit decimal arithmetic (its own exp)."""
+    from decimal import Decimal, localcontext
+    with localcontext() as ctx:
+        ctx.prec = prec
+        gd, ud = Decimal(g), Decimal(u)      # exact conversions of the doubles
+        return float(gd / (1 + (-gd).exp()) * ud)
+
+
+def test_silu_mul_f64_matches_high_precision(orc):
+    """The unrounded float64 silu(g) * u (the value the end-to-end SwiGLU bound
+    is stated around) agrees with 60-digit decimal arithmetic to a few float64
+    ulps, across large, moderate, tiny and zero g and both signs of u."""
+    rng = np.random.default_rng(17)
+    g = np.concatenate([rng.uniform(-40, 40, 2000), rng.standard_normal(500) * 1e-3,
+                        np.array([0.0, -0.0, 1e-7, -1e-7, 3e-12, -2.5e-30, 1e-300, 20.0, -20.0, 2.4, -1.28])])
+    u = rng.standard_normal(g.size) * np.exp(rng.uniform(-8, 8, g.size))
+    got = orc.silu_mul_f64(g, u)
+    for gi, ui, h in zip(g, u, got):
+        want = _exact_silu_mul(float(gi), float(ui))
+        if want == 0.0:
+            assert h == 0.0
+        else:
+            assert abs(h - want) <= 1e-14 * abs(want), (gi, ui, h, want)
