@@ -217,37 +217,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp < kScaleWarp0) {
         setmaxnreg_dec<kRegsCtl>();
-        if (warp == 0 && lane == 0) {
+        // The producer and the MMA issuer run as whole warps: every lane takes
+        // the barrier waits (decided warp-wide), one elected lane issues the
+        // copies / MMAs.  A single-lane loop around bounded waits measured far
+        // slower MMA issue (the tensor pipe then idles between MMAs).
+        if (warp == 0) {
             // ------------------------------------------------------------ producer (both CTAs)
             const uint32_t full_leader = mapa_shared(smem_u32(full), 0);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t fills[kStages] = {};
-            for (int tile = blockIdx.x >> 1; tile < num_tiles && !s_abort && !p.stall; tile += gridDim.x >> 1) {
+            for (int tile = blockIdx.x >> 1; tile < num_tiles && !p.stall; tile += gridDim.x >> 1) {
+                if (__any_sync(0xffffffffu, s_abort != 0)) break;  // warp-uniform exit
                 const int mp = tile / p.n_tiles, nt = tile - mp * p.n_tiles;
                 const int mt = 2 * mp + (int)rank;  // this CTA's 128-row tile of A
+                bool ok = true;
                 for (int kb = 0; kb < p.k_stages; ++kb) {
-                    if (!mbar_wait(&empty[stage], phase ^ 1u, p.wait_ns, p.status, kStatusTimeoutProducer)) {
-                        set_abort();
+                    ok = mbar_wait(&empty[stage], phase ^ 1u, p.wait_ns, p.status, kStatusTimeoutProducer);
+                    if (!__all_sync(0xffffffffu, ok)) {
+                        ok = false;
                         break;
                     }
-                    uint8_t* st = smem + stage * kStageBytes;
-                    const uint32_t bar = full_leader + 8u * (uint32_t)stage;
-                    if (leader) mbar_arrive_expect_tx(&full[stage], kPairTxBytes);
-                    tma_load_2d_pair(st, &tmA, bar, kb * (BK / 2), mt * BM);
-                    tma_load_2d_pair(st + kABytes, &tmB, bar, kb * (BK / 2), nt * BN + (int)rank * (BN / 2));
-                    // Scale tiles as rows of 256 bytes (a 512-byte tile is two rows).
-                    mbar_arrive_expect_tx(&sf_full[stage], kSFABytes + kSFBBytes);
-                    uint8_t* sf = st + kABytes + kBBytes;
-                    tma_load_2d(sf, &tmSFA, &sf_full[stage], 0, (mt * p.kb4 + kb * 4) * 2);
-                    tma_load_2d(sf + kSFABytes, &tmSFB, &sf_full[stage], 0, ((2 * nt) * p.kb4 + kb * 4) * 2);
-                    tma_load_2d(sf + kSFABytes + kSfBox, &tmSFB, &sf_full[stage], 0,
-                                ((2 * nt + 1) * p.kb4 + kb * 4) * 2);
+                    if (elect_one()) {
+                        uint8_t* st = smem + stage * kStageBytes;
+                        const uint32_t bar = full_leader + 8u * (uint32_t)stage;
+                        if (leader) mbar_arrive_expect_tx(&full[stage], kPairTxBytes);
+                        tma_load_2d_pair(st, &tmA, bar, kb * (BK / 2), mt * BM);
+                        tma_load_2d_pair(st + kABytes, &tmB, bar, kb * (BK / 2), nt * BN + (int)rank * (BN / 2));
+                        // Scale tiles as rows of 256 bytes (a 512-byte tile is two rows).
+                        mbar_arrive_expect_tx(&sf_full[stage], kSFABytes + kSFBBytes);
+                        uint8_t* sf = st + kABytes + kBBytes;
+                        tma_load_2d(sf, &tmSFA, &sf_full[stage], 0, (mt * p.kb4 + kb * 4) * 2);
+                        tma_load_2d(sf + kSFABytes, &tmSFB, &sf_full[stage], 0, ((2 * nt) * p.kb4 + kb * 4) * 2);
+                        tma_load_2d(sf + kSFABytes + kSfBox, &tmSFB, &sf_full[stage], 0,
+                                    ((2 * nt + 1) * p.kb4 + kb * 4) * 2);
+                    }
+                    __syncwarp();
                     ++fills[stage];
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
+                }
+                if (!ok) {
+                    if (lane == 0) set_abort();
+                    break;
                 }
             }
             // Drain: every copy into either CTA must land before the pair may exit.
@@ -259,49 +273,62 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (void)mbar_wait(&full[s], (fills[s] - 1u) & 1u, p.wait_ns, p.status, kStatusTimeoutProducer);
                     (void)mbar_wait(&sf_full[s], (fills[s] - 1u) & 1u, p.wait_ns, p.status, kStatusTimeoutProducer);
                 }
-        } else if (warp == 1 && leader && lane == 0) {
+            __syncwarp();
+        } else if (warp == 1 && leader) {
             // ------------------------------------------------------------ MMA issuer (leader)
+            const uint32_t smem_base = smem_u32(smem);
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
-            for (int tile = blockIdx.x >> 1; tile < num_tiles && !s_abort; tile += gridDim.x >> 1) {
-                if (!mbar_wait(acc_empty, acc_phase ^ 1u, p.wait_ns, p.status, kStatusTimeoutMma)) {
-                    set_abort();
+            for (int tile = blockIdx.x >> 1; tile < num_tiles; tile += gridDim.x >> 1) {
+                if (__any_sync(0xffffffffu, s_abort != 0)) break;  // warp-uniform exit
+                bool ok = mbar_wait(acc_empty, acc_phase ^ 1u, p.wait_ns, p.status, kStatusTimeoutMma);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    if (lane == 0) set_abort();
                     break;
                 }
                 tc_fence_after();
-                bool ok = true;
                 for (int kb = 0; kb < p.k_stages; ++kb) {
-                    if (!mbar_wait(&sfready[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma)) {
+                    ok = mbar_wait(&sfready[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma);
+                    if (!__all_sync(0xffffffffu, ok)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const int nk = min(4, p.kb4 - kb * 4);
-                    const uint32_t st = smem_u32(smem + stage * kStageBytes);
-                    const uint32_t sfa_t = tmem + kSfTmem + stage * kSfTmemPerStage;
+                    const uint32_t st = smem_base + (uint32_t)stage * kStageBytes;
+                    // K group j of the stage starts 32 bytes further into each
+                    // 128-byte swizzled row: +2 in the descriptors' address field.
+                    const uint64_t adesc = smem_desc(st, 16, 1024, 2);
+                    const uint64_t bdesc = smem_desc(st + kABytes, 16, 1024, 2);
+                    const uint32_t sfa_t = tmem + kSfTmem + (uint32_t)stage * kSfTmemPerStage;
                     const uint32_t sfb_t = sfa_t + 16;
-                    for (int j = 0; j < nk; ++j) {
-                        const uint64_t adesc = smem_desc(st + 32 * j, 16, 1024, 2);
-                        const uint64_t bdesc = smem_desc(st + kABytes + 32 * j, 16, 1024, 2);
-                        mma_pair_mxf4nvf4(tmem, adesc, bdesc, kIdesc, sfa_t + 4 * j, sfb_t + 8 * j,
-                                          (kb > 0 || j > 0) ? 1u : 0u);
+                    if (elect_one()) {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            if (j < nk)
+                                mma_pair_mxf4nvf4(tmem, adesc + 2u * j, bdesc + 2u * j, kIdesc, sfa_t + 4u * j,
+                                                  sfb_t + 8u * j, (kb > 0 || j > 0) ? 1u : 0u);
+                        tc_commit_pair_mc(&empty[stage], 3);
                     }
-                    tc_commit_pair_mc(&empty[stage], 3);
+                    __syncwarp();
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) {
-                    set_abort();
+                    if (lane == 0) set_abort();
                     break;
                 }
-                tc_commit_pair_mc(acc_full, 3);
+                if (elect_one()) tc_commit_pair_mc(acc_full, 3);
+                __syncwarp();
                 acc_phase ^= 1u;
             }
             // Every issued MMA must finish before TMEM is released.
-            tc_commit_pair(done_bar);
+            if (elect_one()) tc_commit_pair(done_bar);
+            __syncwarp();
             (void)mbar_wait(done_bar, 0u, p.wait_ns, p.status, kStatusTimeoutMma);
+            __syncwarp();
         }
     } else if (warp < kEpiWarp0) {
         // ---------------------------------------------------------------- scale warps (both CTAs)

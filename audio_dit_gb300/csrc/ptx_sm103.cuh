@@ -216,6 +216,18 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p)
     return v;
 }
 
+// One lane of the (fully converged) warp is elected; the others get false.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t e;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(e));
+    return e != 0;
+}
+
 // ------------------------------------------------------------------ clusters / multicast
 
 __device__ __forceinline__ uint32_t cluster_ctarank()

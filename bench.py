@@ -31,7 +31,9 @@ sys.path.insert(0, ROOT)
 METRIC = "fused NVFP4 linear TFLOPS (% GB300 FP4 peak); act-quant GB/s (% HBM), 1 GPU"
 L2_FLUSH_BYTES = 256 << 20
 FP4_OVER_BF16 = 6.0   # nominal dense fp4 / bf16 tensor ratio (13.5 / 2.25 PFLOP/s)
-DEFAULT_CONFIG = "qkv"
+DEFAULT_CONFIG = "fc1"
+L2_BYTES = 129e6  # GB300 L2; an activation below it is re-read from L2 by the pack pass
+CPU_ROWS = {"tiny": 256, "qkv": 256, "fc1": 128, "fc2": 128, "attn_out": 256}  # oracle sample rows per workload
 REFERENCE_BUDGET_S = 120.0  # CPU seconds the reference arm's timed steps aim for in total
 # DRAM bytes (read + write) per launch of nvfp4_gemm_kernel from one ncu capture
 # of the current kernel per workload; None where not captured.
@@ -113,10 +115,10 @@ class ClockSampler:
 class Problem:
     """Device-resident inputs and outputs of one workload."""
 
-    def __init__(self, name: str, torch, A):
+    def __init__(self, name: str, torch, A, data=None):
         import workloads as W
         self.name = name
-        d = W.make_inputs(name)
+        d = W.make_inputs(name) if data is None else data
         self.d = d
         self.M, self.N, self.K = d["M"], d["N"], d["K"]
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
@@ -165,8 +167,17 @@ class Problem:
                        resid=resid, bias=self.bias, seg_off=self.seg_off)
 
     def quant_bytes(self):
+        """Algorithmic HBM bytes of the quantiser: the amax pass reads X (2 B per
+        element); the pack pass reads X again, writes the codes (0.5 B) and the
+        block scales (1/16 B).  The pack pass's read of X counts only where X is
+        larger than L2: a smaller activation is still in L2 from the amax pass.
+        With a caller-given global scale the pack pass is the only pass and its
+        read of X always counts."""
         MK = self.M * self.K
-        return {"amax": 2.0 * MK, "pack": 2.0 * MK + 0.5 * MK + MK / 16.0}
+        x_bytes = 2.0 * MK
+        reread = x_bytes if x_bytes > L2_BYTES else 0.0
+        return {"amax": x_bytes, "pack": reread + 0.5 * MK + MK / 16.0,
+                "pack_given": x_bytes + 0.5 * MK + MK / 16.0}
 
     def gemm_bytes(self):
         MK, NK, MN = self.M * self.K, self.N * self.K, self.M * self.N
@@ -335,6 +346,26 @@ def time_block_graph(torch, A, M: int, steps: int, flush):
     res["graph_tflops"] = round(flops / (res["graph_ms"] * 1e-3) / 1e12, 1)
     res["launches_per_block"] = "12 kernels + 1 memset"
     return res
+
+
+def time_m_sweep(torch, A, steps: int, flush, fp4_peak: float):
+    """The attention-output shape K = N = 3072 (one segment, gate and residual,
+    attn_out value distributions) over M = 1024 ... 65536 tokens: quantiser
+    (in-run amax) + GEMM per step, L2 flushed between steps."""
+    import workloads as W
+    rows = []
+    for M in (1024, 2048, 4096, 8192, 16384, 32768, 65536):
+        pe = Problem("attn_out", torch, A, data=W.m_sweep_inputs(M))
+        q, g, _ = time_device_steps(torch, A, pe, steps, 3, flush)
+        qb = pe.quant_bytes()
+        gt = pe.flops / (np.mean(g) * 1e-3) / 1e12
+        rows.append({"M": M, "tflops": round(pe.flops / (np.mean(q + g) * 1e-3) / 1e12, 1),
+                     "gemm_tflops": round(gt, 1), "gemm_frac_fp4_peak": round(gt / fp4_peak, 4),
+                     "quant_gbs": round((qb["amax"] + qb["pack"]) / (np.mean(q) * 1e-3) / 1e9, 1),
+                     "ms_per_step": round(float(np.mean(q + g)), 4)})
+        del pe
+        torch.cuda.empty_cache()
+    return rows
 
 
 def time_device_steps(torch, A, prob: Problem, steps: int, warmup: int, flush, given_scale: bool = False):
@@ -547,12 +578,12 @@ def run_gpu(args):
         qg, gg, _ = time_device_steps(torch, A, prob, max(5, min(500, args.steps // 4)), 3, flush, given_scale=True)
         given = {"tflops": round(prob.flops / (np.mean(qg + gg) * 1e-3) / 1e12, 1),
                  "quant_ms": round(float(np.mean(qg)), 5),
-                 "quant_gbs": round(qb["pack"] / (np.mean(qg) * 1e-3) / 1e9, 1),
+                 "quant_gbs": round(qb["pack_given"] / (np.mean(qg) * 1e-3) / 1e9, 1),
                  "note": "global scale supplied by the caller: pack pass + GEMM"}
 
     extra = {}
     if rank == 0 and not args.no_extra:
-        for name in [c for c in ["tiny", "fc1", "fc2", "attn_out"] if c != args.config]:
+        for name in [c for c in ["tiny", "qkv", "fc1", "fc2", "attn_out"] if c != args.config]:
             try:
                 pe = Problem(name, torch, A)
                 qe, ge, _ = time_device_steps(torch, A, pe, max(5, min(200, args.steps // 4)), 3, flush)
@@ -566,12 +597,16 @@ def run_gpu(args):
                     "quant_gbs": round((qbe["amax"] + qbe["pack"]) / (np.mean(qe) * 1e-3) / 1e9, 1),
                     "ms_per_step": round(float(np.mean(qe + ge)), 4),
                     "given_scale_tflops": round(pe.flops / (np.mean(qge + gge) * 1e-3) / 1e12, 1),
-                    "given_scale_quant_gbs": round(qbe["pack"] / (np.mean(qge) * 1e-3) / 1e9, 1),
+                    "given_scale_quant_gbs": round(qbe["pack_given"] / (np.mean(qge) * 1e-3) / 1e9, 1),
                 }
                 del pe
                 torch.cuda.empty_cache()
             except Exception as e:  # a failing extra config must not hide the headline
                 extra[name] = {"error": repr(e)[:200]}
+        try:
+            extra["m_sweep"] = time_m_sweep(torch, A, max(5, min(100, args.steps // 20)), flush, fp4_peak)
+        except Exception as e:
+            extra["m_sweep"] = {"error": repr(e)[:200]}
         try:
             extra["mlp_swiglu"] = time_mlp_chain(torch, A, max(3, min(50, args.steps // 40)), 3, flush)
             extra["mlp_swiglu"]["fc1_swiglu_gemm_frac_fp4_peak"] = round(
@@ -587,11 +622,21 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rows = args.cpu_rows
-        tf, dt, cores, split = oracle_sample(args.config, rows)
-        cpu = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "split": split,
-               "sample": f"first {rows} rows of {args.config} (own amax), all {rows}x{prob.N} outputs in "
-                         f"float64, W quantised once beforehand; {dt:.1f} s"}
+        def cpu_line(name, rows):
+            tf, dt, cores, split = oracle_sample(name, rows)
+            wl = W.WORKLOADS[name]
+            return {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "split": split,
+                    "sample": f"first {rows} rows of {name} (own amax), all {rows}x{wl.N} outputs in "
+                              f"float64, W quantised once beforehand; {dt:.1f} s"}
+        import workloads as W
+        cpu = cpu_line(args.config, args.cpu_rows or CPU_ROWS[args.config])
+        if not args.no_extra:
+            for name in [c for c in CPU_ROWS if c != args.config]:
+                if name in extra and "error" not in extra[name]:
+                    try:
+                        extra[name]["cpu_baseline"] = cpu_line(name, CPU_ROWS[name])
+                    except Exception as e:
+                        extra[name]["cpu_baseline"] = {"error": repr(e)[:200]}
 
     if rank == 0:
         line = {
@@ -625,7 +670,9 @@ def run_gpu(args):
                          "traffic": NCU_GEMM_TRAFFIC.get(args.config), "algorithmic_bytes": prob.gemm_bytes()},
             "quant": {"gbs": round(quant_gbs, 1), "peak_gbs": peaks["hbm_gbs"],
                       "frac": round(quant_gbs / peaks["hbm_gbs"], 4), "ms": round(quant_ms, 5),
-                      "bytes": "amax read 2 B/elem + pack read 2 + codes 0.5 + scales 1/16 B/elem"},
+                      "bytes": "amax read 2 B/elem + pack re-read of X 2 B/elem (only where X exceeds L2) "
+                               "+ codes 0.5 + scales 1/16 B/elem",
+                      "algorithmic_bytes": qb["amax"] + qb["pack"]},
             "gemm_ms": round(gemm_ms, 5),
             "timing": {"gemm_ms_median": round(float(np.median(g)), 5), "gemm_ms_best": round(float(np.min(g)), 5),
                        "quant_ms_median": round(float(np.median(q)), 5), "quant_ms_best": round(float(np.min(q)), 5),
@@ -661,7 +708,7 @@ def run_reference(args):
     import workloads as W
     import oracle
     oracle.build()
-    max_rows = args.cpu_rows
+    max_rows = args.cpu_rows or CPU_ROWS[args.config]
     sample = OracleSample(args.config, max_rows)
     per_row = []
     for _ in range(args.warmup):
@@ -707,7 +754,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=["tiny", "qkv", "fc1", "fc2", "attn_out"])
-    ap.add_argument("--cpu-rows", type=int, default=256)
+    ap.add_argument("--cpu-rows", type=int, default=0, help="oracle sample rows (0: per-workload default)")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
