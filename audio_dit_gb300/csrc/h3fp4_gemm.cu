@@ -29,21 +29,23 @@
 // So four "scale warps", one per lane quarter, load each stage's 512-byte
 // scale tiles from shared memory and store them into their quarter.
 //
-// Roles (512 threads per CTA in four warpgroups, persistent over pair tiles):
-//   warp 0      TMA producer (both CTAs): A / W code tiles (128-byte swizzle)
-//               complete on the LEADER's "full" barrier of the stage; this
-//               CTA's block-scale tiles complete on its own "scales landed"
-//               barrier (5-stage ring).
-//   warp 1      TMEM owner (both) + MMA issuer (leader): per stage, one wait
-//               on the leader's "scales ready", four paired MMAs, then a commit
+// Roles (512 threads per CTA in four warpgroups, persistent over pair tiles).
+// The producer and the MMA issuer run as whole warps -- every lane takes the
+// barrier waits, one elected lane issues -- because a single-lane loop around
+// bounded waits measured about 2.2x slower MMA issue (the tensor pipe idles):
+//   warp 0      TMA producer (both CTAs): per stage first this CTA's
+//               block-scale tiles (on its own "scales landed" barrier), then
+//               the A / W code tiles (128-byte swizzle), which complete on the
+//               LEADER's "full" barrier (5-stage ring).
+//   warp 1      TMEM owner (both) + MMA issuer (leader): per stage, waits on
+//               the leader's "full" (both CTAs' code tiles) and "scales ready"
+//               (both CTAs' scales in TMEM), four paired MMAs, then a commit
 //               multicast to both CTAs' "empty" barrier.
 //   warps 4-7   scale warps (both), warp 4 + q serving lane quarter q: per
-//               stage twelve 16-byte shared loads per lane, tcgen05.st of 48
-//               columns, then an arrival on the leader's "scales ready".  The
-//               leader's scale warps arrive only after the stage's code tiles
-//               of both CTAs landed too, so "scales ready" alone clears a stage
-//               for the MMAs: every wait in the issuing thread stalls the
-//               tensor pipe (about 75 cycles per extra wait per 513-cycle stage).
+//               stage, as soon as the CTA's scale tiles landed, twelve 16-byte
+//               shared loads per lane, tcgen05.st of 48 columns, then an
+//               arrival on the leader's "scales ready" -- overlapping the code
+//               tiles' transfer.
 //   warps 8-15  epilogue (both): tcgen05.ld the CTA's 128 x 256 fp32
 //               accumulator (each warp 32 rows x 128 columns), release it to
 //               the leader, then alpha/bias/gate/residual on paired fp32
@@ -167,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);  // leader's: both CTAs' code tiles
     uint64_t* empty = full + kStages;                                // both: the MMAs released the stage
     uint64_t* sf_full = empty + kStages;                             // both: this CTA's scale tiles landed
-    uint64_t* sfready = sf_full + kStages;  // leader's: both CTAs' scales in TMEM and code tiles landed
+    uint64_t* sfready = sf_full + kStages;  // leader's: both CTAs' scales in TMEM
     uint64_t* acc_full = sfready + kStages;                          // both: accumulator complete
     uint64_t* acc_empty = acc_full + 1;                              // leader's: both epilogues drained
     uint64_t* rbar = acc_empty + 1;                                  // one per epilogue warp
@@ -240,17 +242,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (elect_one()) {
                         uint8_t* st = smem + stage * kStageBytes;
-                        const uint32_t bar = full_leader + 8u * (uint32_t)stage;
-                        if (leader) mbar_arrive_expect_tx(&full[stage], kPairTxBytes);
-                        tma_load_2d_pair(st, &tmA, bar, kb * (BK / 2), mt * BM);
-                        tma_load_2d_pair(st + kABytes, &tmB, bar, kb * (BK / 2), nt * BN + (int)rank * (BN / 2));
-                        // Scale tiles as rows of 256 bytes (a 512-byte tile is two rows).
+                        // Scale tiles first (as rows of 256 bytes; a 512-byte tile is
+                        // two rows): the scale warps move them into TMEM while the
+                        // code tiles are still arriving.
                         mbar_arrive_expect_tx(&sf_full[stage], kSFABytes + kSFBBytes);
                         uint8_t* sf = st + kABytes + kBBytes;
                         tma_load_2d(sf, &tmSFA, &sf_full[stage], 0, (mt * p.kb4 + kb * 4) * 2);
                         tma_load_2d(sf + kSFABytes, &tmSFB, &sf_full[stage], 0, ((2 * nt) * p.kb4 + kb * 4) * 2);
                         tma_load_2d(sf + kSFABytes + kSfBox, &tmSFB, &sf_full[stage], 0,
                                     ((2 * nt + 1) * p.kb4 + kb * 4) * 2);
+                        const uint32_t bar = full_leader + 8u * (uint32_t)stage;
+                        if (leader) mbar_arrive_expect_tx(&full[stage], kPairTxBytes);
+                        tma_load_2d_pair(st, &tmA, bar, kb * (BK / 2), mt * BM);
+                        tma_load_2d_pair(st + kABytes, &tmB, bar, kb * (BK / 2), nt * BN + (int)rank * (BN / 2));
                     }
                     __syncwarp();
                     ++fills[stage];
@@ -288,7 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 for (int kb = 0; kb < p.k_stages; ++kb) {
-                    ok = mbar_wait(&sfready[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma);
+                    // Both CTAs' code tiles in shared memory, both CTAs' scales in TMEM.
+                    ok = mbar_wait(&full[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma) &&
+                         mbar_wait(&sfready[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma);
                     if (!__all_sync(0xffffffffu, ok)) {
                         ok = false;
                         break;
@@ -351,8 +357,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 ok = mbar_wait(&sf_full[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma);
-                // The leader's arrival also vouches for both CTAs' code tiles.
-                if (ok && leader) ok = mbar_wait(&full[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma);
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;

@@ -136,7 +136,7 @@ __device__ __forceinline__ int segment_of(const Segments& s, long long r)
 // Per-thread modulation constants for the 16 columns it owns.
 struct ModCols {
     uint64_t onep[8], sh[8];  // (1 + scale, shift) of columns 2j, 2j + 1
-    long long seg_end;
+    long long seg_begin, seg_end;  // rows [seg_begin, seg_end) use these constants
 };
 
 __device__ __forceinline__ void load_mod(const QuantParams& p, int seg, int cb, ModCols& mc)
@@ -152,6 +152,7 @@ __device__ __forceinline__ void load_mod(const QuantParams& p, int seg, int cb, 
         mc.sh[2 * i] = f2(b.x, b.y);
         mc.sh[2 * i + 1] = f2(b.z, b.w);
     }
+    mc.seg_begin = p.seg.off[seg];
     mc.seg_end = p.seg.off[seg + 1];
 }
 
@@ -162,6 +163,7 @@ __device__ __forceinline__ void init_mod(ModCols& mc)
         mc.onep[j] = f2(1.0f, 1.0f);
         mc.sh[j] = f2(0.0f, 0.0f);
     }
+    mc.seg_begin = 0;
     mc.seg_end = -1;
 }
 
@@ -275,7 +277,11 @@ __global__ void __launch_bounds__(kThreads, 10) pack_kernel(QuantParams p)
 
     ModCols mc;
     init_mod(mc);
-    for (long long r = r0; r < r1; r += kRowUnroll) {
+    // Rows are walked from the end of the CTA's range back to its start: the
+    // amax pass walked them forwards, so the rows it read last -- the ones most
+    // likely still in L2 when X is larger than L2 -- are re-read first.
+    const long long last = r1 > r0 ? r0 + (r1 - r0 - 1) / kRowUnroll * kRowUnroll : r0 - kRowUnroll;
+    for (long long r = last; r >= r0; r -= kRowUnroll) {
         V16 v[kRowUnroll];
 #pragma unroll
         for (int u = 0; u < kRowUnroll; ++u) {
@@ -291,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 10) pack_kernel(QuantParams p)
             float f[16];
             unpack16(v[u], f);
             if (kMod && real) {
-                if (rr >= mc.seg_end && valid) load_mod(p, segment_of(p.seg, rr), cb, mc);
+                if ((rr >= mc.seg_end || rr < mc.seg_begin) && valid) load_mod(p, segment_of(p.seg, rr), cb, mc);
                 modulate16<kMod>(f, mc);
             }
             float bmax = 0.0f;
