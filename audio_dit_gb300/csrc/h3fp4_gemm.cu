@@ -35,17 +35,18 @@
 // bounded waits measured about 2.2x slower MMA issue (the tensor pipe idles):
 //   warp 0      TMA producer (both CTAs): per stage first this CTA's
 //               block-scale tiles (on its own "scales landed" barrier), then
-//               the A / W code tiles (128-byte swizzle), which complete on the
-//               LEADER's "full" barrier (5-stage ring).
-//   warp 1      TMEM owner (both) + MMA issuer (leader): per stage, waits on
-//               the leader's "full" (both CTAs' code tiles) and "scales ready"
-//               (both CTAs' scales in TMEM), four paired MMAs, then a commit
+//               the A / W code tiles (128-byte swizzle), whose bytes complete
+//               on the LEADER's "full" barrier (5-stage ring).
+//   warp 1      TMEM owner (both) + MMA issuer (leader): per stage, one wait
+//               on the leader's "full", four paired MMAs, then a commit
 //               multicast to both CTAs' "empty" barrier.
 //   warps 4-7   scale warps (both), warp 4 + q serving lane quarter q: per
 //               stage, as soon as the CTA's scale tiles landed, twelve 16-byte
 //               shared loads per lane, tcgen05.st of 48 columns, then an
-//               arrival on the leader's "scales ready" -- overlapping the code
-//               tiles' transfer.
+//               arrival on the leader's "full" -- overlapping the code tiles'
+//               transfer.  "full" therefore completes when both CTAs' code
+//               tiles landed (transaction bytes) and all eight scale warps
+//               arrived: a single wait per stage in the issuing warp.
 //   warps 8-15  epilogue (both): tcgen05.ld the CTA's 128 x 256 fp32
 //               accumulator (each warp 32 rows x 128 columns), release it to
 //               the leader, then alpha/bias/gate/residual on paired fp32
@@ -96,7 +97,7 @@ constexpr uint32_t kChunkBytes = 32 * 32 * 2;         // 32 rows x 32 bf16
 constexpr uint32_t kEpiWarpBytes = 2 * kChunkBytes;   // 4096: two staging buffers
 constexpr uint32_t kEpiOff = kStages * kStageBytes;
 constexpr uint32_t kBarOff = kEpiOff + kEpiWarps * kEpiWarpBytes;
-constexpr uint32_t kBarBytes = 8 * (4 * kStages + 3 + kEpiWarps) + 8;  // barriers, TMEM address, abort flag
+constexpr uint32_t kBarBytes = 8 * (3 * kStages + 3 + kEpiWarps) + 8;  // barriers, TMEM address, abort flag
 constexpr uint32_t kSmemBytes = kBarOff + 512;
 static_assert(kBarBytes <= 512, "barrier block");
 constexpr uint32_t kTmemCols = 512;
@@ -166,11 +167,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const uint32_t rank = cluster_ctarank();  // 0 = leader (issues the MMAs)
     const bool leader = rank == 0;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);  // leader's: both CTAs' code tiles
+    // Leader's "full": both CTAs' code tiles landed (tx bytes) AND the eight
+    // scale warps of the pair stored the stage's scales in TMEM (arrivals), so
+    // one wait clears a stage for the MMAs.
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
     uint64_t* empty = full + kStages;                                // both: the MMAs released the stage
     uint64_t* sf_full = empty + kStages;                             // both: this CTA's scale tiles landed
-    uint64_t* sfready = sf_full + kStages;  // leader's: both CTAs' scales in TMEM
-    uint64_t* acc_full = sfready + kStages;                          // both: accumulator complete
+    uint64_t* acc_full = sf_full + kStages;                          // both: accumulator complete
     uint64_t* acc_empty = acc_full + 1;                              // leader's: both epilogues drained
     uint64_t* rbar = acc_empty + 1;                                  // one per epilogue warp
     uint64_t* done_bar = rbar + kEpiWarps;
@@ -180,10 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         s_abort = 0;
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 1 + 2 * 4);  // the producer's expect_tx + four scale warps per CTA
             mbar_init(&empty[s], 1);
             mbar_init(&sf_full[s], 1);
-            mbar_init(&sfready[s], 2 * 4);  // four scale warps in each CTA
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 2 * kEpiWarps);
@@ -293,8 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 for (int kb = 0; kb < p.k_stages; ++kb) {
                     // Both CTAs' code tiles in shared memory, both CTAs' scales in TMEM.
-                    ok = mbar_wait(&full[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma) &&
-                         mbar_wait(&sfready[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma);
+                    ok = mbar_wait(&full[stage], phase, p.wait_ns, p.status, kStatusTimeoutMma);
                     if (!__all_sync(0xffffffffu, ok)) {
                         ok = false;
                         break;
@@ -346,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // i.e. after the MMAs that read the previous contents committed.
         setmaxnreg_dec<kRegsScale>();
         const uint32_t q = (uint32_t)(warp & 3);
-        const uint32_t ready_leader = mapa_shared(smem_u32(sfready), 0);
+        const uint32_t ready_leader = mapa_shared(smem_u32(full), 0);
         int stage = 0;
         uint32_t phase = 0;
         for (int tile = blockIdx.x >> 1; tile < num_tiles; tile += gridDim.x >> 1) {

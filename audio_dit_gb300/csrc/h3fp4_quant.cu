@@ -251,6 +251,7 @@ template <bool kMod, bool kWide>
 __global__ void __launch_bounds__(kThreads, 10) pack_kernel(QuantParams p)
 {
     __shared__ float red[kThreads / 32];
+    __shared__ float rcp_tab[128];  // E4M3 code S -> RN(1 / RN(S * s)), 0 for S = 0
     griddep_launch_dependents();
     griddep_wait();  // the amax partials (or the given scale) come from the previous kernel
     // Global scale: one full-activation amax over every partial of pass 1.
@@ -264,6 +265,15 @@ __global__ void __launch_bounds__(kThreads, 10) pack_kernel(QuantParams p)
         s_g = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 2688.0f);
         if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *p.gscale = s_g;
     }
+    // The effective scale eff = S * s and its reciprocal depend only on the
+    // block's E4M3 code S (127 finite non-negative values; the saturating
+    // conversion never yields the NaN code 0x7F): one table per CTA instead of
+    // a multiply and an IEEE reciprocal per block.
+    for (int c = threadIdx.x; c < 128; c += kThreads) {
+        const float eff = __fmul_rn(e4m3_value((uint32_t)c), s_g);
+        rcp_tab[c] = (eff == 0.0f || c == 0x7F) ? 0.0f : fminf(__frcp_rn(eff), FLT_MAX);
+    }
+    __syncthreads();
 
     const int lane = threadIdx.x & 31;
     const int cb = blockIdx.x * kThreads + threadIdx.x;
@@ -271,58 +281,64 @@ __global__ void __launch_bounds__(kThreads, 10) pack_kernel(QuantParams p)
     const long long kb4 = p.K / 64;             // scale tiles per 128 rows
     const long long r0 = (long long)blockIdx.y * p.rows_per_cta;
     const long long r1 = min(r0 + (long long)p.rows_per_cta, p.rows_pad);
-    const uint16_t* xc = p.x + (long long)cb * 16;
+    const long long rend = min(r1, p.rows);      // real rows [r0, rend), padding rows [rend, r1)
+    // Lanes past the last block column load column 0 (in bounds) and store nothing.
+    const uint16_t* xc = p.x + (long long)(valid ? cb : 0) * 16;
     uint2* codes_c = reinterpret_cast<uint2*>(p.codes) + cb;  // 8 bytes per block
     const long long g = cb >> 2;                 // 64-column group = scale word index
+    const bool sf_writer = valid && (lane & 3) == 0;
 
     ModCols mc;
     init_mod(mc);
     // Rows are walked from the end of the CTA's range back to its start: the
     // amax pass walked them forwards, so the rows it read last -- the ones most
     // likely still in L2 when X is larger than L2 -- are re-read first.
-    const long long last = r1 > r0 ? r0 + (r1 - r0 - 1) / kRowUnroll * kRowUnroll : r0 - kRowUnroll;
+    const long long last = rend > r0 ? r0 + (rend - r0 - 1) / kRowUnroll * kRowUnroll : r0 - kRowUnroll;
     for (long long r = last; r >= r0; r -= kRowUnroll) {
         V16 v[kRowUnroll];
 #pragma unroll
-        for (int u = 0; u < kRowUnroll; ++u) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[u].w[i] = 0u;
-            if (valid && r + u < r1 && r + u < p.rows) v[u] = ld16<kWide>(xc + (r + u) * p.K);
-        }
+        for (int u = 0; u < kRowUnroll; ++u)
+            if (r + u < rend) v[u] = ld16<kWide>(xc + (r + u) * p.K);
 #pragma unroll
         for (int u = 0; u < kRowUnroll; ++u) {
             const long long rr = r + u;
-            if (rr >= r1) break;                   // uniform over the CTA
-            const bool real = rr < p.rows;
+            if (rr >= rend) break;                 // uniform over the CTA
             float f[16];
             unpack16(v[u], f);
-            if (kMod && real) {
+            if (kMod) {
                 if ((rr >= mc.seg_end || rr < mc.seg_begin) && valid) load_mod(p, segment_of(p.seg, rr), cb, mc);
                 modulate16<kMod>(f, mc);
             }
             float bmax = 0.0f;
 #pragma unroll
             for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, fabsf(f[j]));
-            const uint32_t S = real ? cvt_e4m3(__fdiv_rn(div6_bf16(bmax), s_g)) : 0u;
-            const float eff = __fmul_rn(e4m3_value(S), s_g);
-            const float rcp = (eff == 0.0f) ? 0.0f : fminf(__frcp_rn(eff), FLT_MAX);
+            const uint32_t S = cvt_e4m3(__fdiv_rn(div6_bf16(bmax), s_g));
+            const float rcp = rcp_tab[S & 127u];
             const uint64_t rcp2 = f2(rcp, rcp);
             float q[16];
 #pragma unroll
             for (int j = 0; j < 8; ++j) unf2(mul2(f2(f[2 * j], f[2 * j + 1]), rcp2), q[2 * j], q[2 * j + 1]);
             const uint32_t w0 = e2m1x8(reinterpret_cast<const float(&)[8]>(q[0]));
             const uint32_t w1 = e2m1x8(reinterpret_cast<const float(&)[8]>(q[8]));
-            if (valid && real) codes_c[rr * (p.K / 16)] = make_uint2(w0, w1);
+            if (valid) codes_c[rr * (p.K / 16)] = make_uint2(w0, w1);
             // gather the four block scales of this 64-column group into lane%4 == 0
             const uint32_t s1 = __shfl_down_sync(0xffffffffu, S, 1);
             const uint32_t s2 = __shfl_down_sync(0xffffffffu, S, 2);
             const uint32_t s3 = __shfl_down_sync(0xffffffffu, S, 3);
-            if (valid && (lane & 3) == 0) {
-                const long long off = (((rr >> 7) * kb4 + g) << 9) + ((rr & 31) << 4) + (((rr >> 5) & 3) << 2);
+            if (sf_writer) {
+                const uint32_t r7 = (uint32_t)rr & 127u;
+                const long long off = (((rr >> 7) * kb4 + g) << 9) + ((r7 & 31u) << 4) + ((r7 >> 5) << 2);
                 *reinterpret_cast<uint32_t*>(p.sf + off) = S | (s1 << 8) | (s2 << 16) | (s3 << 24);
             }
         }
     }
+    // Padding rows up to the next multiple of 128: zero scale words.
+    if (sf_writer)
+        for (long long rr = max(r0, rend); rr < r1; ++rr) {
+            const uint32_t r7 = (uint32_t)rr & 127u;
+            const long long off = (((rr >> 7) * kb4 + g) << 9) + ((r7 & 31u) << 4) + ((r7 >> 5) << 2);
+            *reinterpret_cast<uint32_t*>(p.sf + off) = 0u;
+        }
 }
 
 // One CTA: max over the amax partials of pass 1 -> *out (the tensor amax).
