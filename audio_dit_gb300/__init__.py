@@ -22,7 +22,7 @@ __all__ = [
     "MAX_SEGMENTS", "library_path", "load_library", "h3fp4_codes_bytes", "h3fp4_sf_bytes",
     "h3fp4_workspace_bytes", "h3fp4_quantize_weight", "h3fp4_quantize_act", "h3fp4_linear",
     "h3fp4_check", "h3fp4_act_amax", "h3fp4_gscale_from_amax", "h3fp4_selftest_timeout", "h3fp4_measure_fp4_peak", "h3fp4_measure_fp4_pair_peak", "h3fp4_quantize_act_noalloc",
-    "h3fp4_set_wait_limit_ns", "h3fp4_status_string", "alloc_nvfp4", "alloc_workspace",
+    "h3fp4_linear_swiglu_nvfp4", "h3fp4_set_wait_limit_ns", "h3fp4_status_string", "alloc_nvfp4", "alloc_workspace",
 ]
 
 PROLOGUE_MOD = 1
@@ -67,6 +67,8 @@ def load_library():
         "h3fp4_linear": (i32, [vp, vp, vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp,
                                i32, vp, vp]),
         "h3fp4_act_amax": (i32, [vp, i64, i64, vp, vp, vp, i32, vp, i32, vp, vp]),
+        "h3fp4_linear_swiglu_nvfp4": (i32, [vp, vp, vp, i64, i64, i64, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp,
+                                            i32, vp, vp]),
         "h3fp4_gscale_from_amax": (i32, [vp, vp, vp]),
         "h3fp4_ws_out_amax": (vp, [vp]),
         "h3fp4_selftest_timeout": (i32, [vp, C.c_uint64, vp]),
@@ -196,6 +198,32 @@ def h3fp4_linear(x: torch.Tensor, w_codes: torch.Tensor, w_sf: torch.Tensor, w_g
         _ptr(bias, "bias", torch.bfloat16), _ptr(resid, "resid", torch.bfloat16),
         _ptr(out, "out", torch.bfloat16), flags, _ptr(ws, "ws", torch.uint8), _stream(stream)),
         "h3fp4_linear")
+
+
+def h3fp4_linear_swiglu_nvfp4(x: torch.Tensor, w_codes: torch.Tensor, w_sf: torch.Tensor, w_gscale: torch.Tensor,
+                              h_codes: torch.Tensor, h_sf: torch.Tensor, h_gscale: torch.Tensor, ws: torch.Tensor, *,
+                              a_sf: Optional[torch.Tensor] = None, a_gscale: Optional[torch.Tensor] = None,
+                              shift: Optional[torch.Tensor] = None, scale: Optional[torch.Tensor] = None,
+                              bias: Optional[torch.Tensor] = None, seg_off: Optional[Sequence[int]] = None,
+                              gscale_given: bool = False, stream=None) -> None:
+    """FC1 with the SwiGLU producer writing h = bf16(silu(g) * u) as NVFP4:
+    ``h_codes`` uint8 [M, N/4], ``h_sf`` (h3fp4_sf_bytes(M, N/2)) under the
+    given global scale ``h_gscale`` (device fp32 [1], an input)."""
+    prequant = x.dtype == torch.uint8
+    M = x.shape[0]
+    K = x.shape[1] * (2 if prequant else 1)
+    N = h_codes.shape[1] * 4
+    flags = ((A_PREQUANT if prequant else 0) | (PROLOGUE_MOD if shift is not None else 0)
+             | (EPI_BIAS if bias is not None else 0) | (GSCALE_GIVEN if gscale_given else 0))
+    sp, nseg, _keep = _segs(seg_off)
+    _check(load_library().h3fp4_linear_swiglu_nvfp4(
+        _ptr(x, "x"), _ptr(a_sf, "a_sf", torch.uint8), _ptr(a_gscale, "a_gscale", torch.float32), M, N, K,
+        _ptr(w_codes, "w_codes", torch.uint8), _ptr(w_sf, "w_sf", torch.uint8),
+        _ptr(w_gscale, "w_gscale", torch.float32), _ptr(shift, "shift", torch.float32),
+        _ptr(scale, "scale", torch.float32), sp, nseg, _ptr(bias, "bias", torch.bfloat16),
+        _ptr(h_gscale, "h_gscale", torch.float32), _ptr(h_codes, "h_codes", torch.uint8),
+        _ptr(h_sf, "h_sf", torch.uint8), flags, _ptr(ws, "ws", torch.uint8), _stream(stream)),
+        "h3fp4_linear_swiglu_nvfp4")
 
 
 def h3fp4_quantize_act_noalloc(x: torch.Tensor, codes: torch.Tensor, sf: torch.Tensor, gscale: torch.Tensor,

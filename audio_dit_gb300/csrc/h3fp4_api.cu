@@ -261,6 +261,77 @@ h3fp4_status h3fp4_linear(const void* x, const void* a_sf, const float* a_gscale
     return from_cuda(launch_gemm(g, stream));
 }
 
+h3fp4_status h3fp4_linear_swiglu_nvfp4(const void* x, const void* a_sf, const float* a_gscale, int64_t M, int64_t N,
+                                       int64_t K, const void* w_codes, const void* w_sf, const float* w_gscale,
+                                       const float* shift, const float* scale, const int64_t* seg_off, int nseg,
+                                       const void* bias_bf16, const float* h_gscale, void* h_codes, void* h_sf,
+                                       int flags, void* ws, cudaStream_t stream)
+{
+    h3fp4_status st = check_shape(M, K);
+    if (st != H3FP4_OK) return st;
+    if (N < 256 || N % 256 != 0 || N > (int64_t)INT32_MAX) return H3FP4_ERR_SHAPE;
+    const int known = H3FP4_PROLOGUE_MOD | H3FP4_EPI_BIAS | H3FP4_GSCALE_GIVEN | H3FP4_A_PREQUANT;
+    if (flags & ~known) return H3FP4_ERR_INVALID;
+    const bool prequant = (flags & H3FP4_A_PREQUANT) != 0;
+    const bool mod = (flags & H3FP4_PROLOGUE_MOD) != 0;
+    const bool bias = (flags & H3FP4_EPI_BIAS) != 0;
+    const bool given = (flags & H3FP4_GSCALE_GIVEN) != 0;
+    if (!x || !w_codes || !w_sf || !w_gscale || !h_gscale || !h_codes || !h_sf || !ws) return H3FP4_ERR_INVALID;
+    if (prequant && (mod || !a_sf || !a_gscale)) return H3FP4_ERR_INVALID;
+    if (given && !a_gscale) return H3FP4_ERR_INVALID;
+    if (mod && (!shift || !scale)) return H3FP4_ERR_INVALID;
+    if (bias && !bias_bf16) return H3FP4_ERR_INVALID;
+    if (h_codes == x || h_codes == w_codes || h_sf == w_sf) return H3FP4_ERR_INVALID;
+    if (!aligned16(x) || !aligned16(w_codes) || !aligned16(w_sf) || !aligned16(h_codes) || !aligned16(h_sf) ||
+        !aligned16(ws) || (reinterpret_cast<uintptr_t>(h_gscale) & 3u) || (prequant && !aligned16(a_sf)) ||
+        (bias && !aligned16(bias_bf16)) || (mod && (!aligned16(shift) || !aligned16(scale))))
+        return H3FP4_ERR_ALIGN;
+    Segments seg;
+    st = make_segments(seg_off, nseg <= 0 ? 1 : nseg, M, &seg);
+    if (st != H3FP4_OK) return st;
+    if ((st = check_device()) != H3FP4_OK) return st;
+
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    GemmJob g{};
+    if (prequant) {
+        g.a_codes = static_cast<const uint8_t*>(x);
+        g.a_sf = static_cast<const uint8_t*>(a_sf);
+        g.a_gscale = a_gscale;
+    } else {
+        QuantJob q{};
+        q.x = x;
+        q.rows = M;
+        q.K = K;
+        q.shift = mod ? shift : nullptr;
+        q.scale = mod ? scale : nullptr;
+        q.seg = seg;
+        q.codes = wsb + kWsActCodes;
+        q.sf = q.codes + round256(h3fp4_codes_bytes(M, K));
+        q.gscale = given ? const_cast<float*>(a_gscale) : reinterpret_cast<float*>(wsb + kWsActGscale);
+        q.gscale_given = given;
+        q.partials = reinterpret_cast<float*>(wsb + kWsPartials);
+        if ((st = from_cuda(launch_quantize(q, stream))) != H3FP4_OK) return st;
+        g.a_codes = q.codes;
+        g.a_sf = q.sf;
+        g.a_gscale = q.gscale;
+    }
+    g.w_codes = static_cast<const uint8_t*>(w_codes);
+    g.w_sf = static_cast<const uint8_t*>(w_sf);
+    g.w_gscale = w_gscale;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.bias = bias ? bias_bf16 : nullptr;
+    g.seg = seg;
+    g.status = reinterpret_cast<unsigned int*>(wsb + kWsStatus);
+    g.wait_limit_ns = g_wait_limit_ns.load();
+    g.swiglu = true;
+    g.h_codes = static_cast<uint8_t*>(h_codes);
+    g.h_sf = static_cast<uint8_t*>(h_sf);
+    g.h_gscale = h_gscale;
+    return from_cuda(launch_gemm(g, stream));
+}
+
 float* h3fp4_ws_out_amax(void* ws)
 {
     return ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kWsOutAmax) : nullptr;

@@ -72,6 +72,7 @@
 
 #include "h3fp4_internal.h"
 #include "ptx_sm103.cuh"
+#include "nvfp4_encode.cuh"
 
 namespace h3fp4 {
 namespace {
@@ -98,7 +99,8 @@ constexpr uint32_t kEpiWarpBytes = 2 * kChunkBytes;   // 4096: two staging buffe
 constexpr uint32_t kEpiOff = kStages * kStageBytes;
 constexpr uint32_t kBarOff = kEpiOff + kEpiWarps * kEpiWarpBytes;
 constexpr uint32_t kBarBytes = 8 * (3 * kStages + 3 + kEpiWarps) + 8;  // barriers, TMEM address, abort flag
-constexpr uint32_t kSmemBytes = kBarOff + 512;
+constexpr uint32_t kRcpOff = kBarOff + 512;             // kNvfp4: 128 fp32 block reciprocals of h
+constexpr uint32_t kSmemBytes = kRcpOff + 512;
 static_assert(kBarBytes <= 512, "barrier block");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmem = 256;
@@ -126,6 +128,11 @@ struct GemmParams {
     unsigned long long wait_ns;
     int stall;  // self-test: the producer issues nothing, so every consumer wait must time out
     float* amax_out;  // kAmax: atomic max of |out| (bf16 values, as fp32 bits) over the call
+    // kNvfp4: h written as NVFP4 under the caller's global scale of h
+    uint8_t* h_codes;      // [M][N/4] bytes
+    uint8_t* h_sf;         // block scales of h, 128x4-tiled, sf_bytes(M, N/2)
+    const float* h_gscale; // device fp32
+    int h_kb4;             // N/2/64 scale groups per row of h
 };
 
 __device__ __forceinline__ int segment_of_row(const Segments& s, int r)
@@ -146,9 +153,11 @@ __device__ __forceinline__ uint32_t swz64(uint32_t r, uint32_t j)
 
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
-// kSwiglu: SwiGLU epilogue (out [M][N/2]); kAmax: track max |out| into p.amax_out.
-// Compile-time, so that the plain epilogue carries neither.
-template <bool kSwiglu, bool kAmax>
+// kSwiglu: SwiGLU epilogue (out [M][N/2]); kAmax: track max |out| into p.amax_out;
+// kNvfp4 (with kSwiglu): h is not stored in bf16 but quantised to NVFP4 under the
+// given global scale of h, with the quantiser's arithmetic (nvfp4_encode.cuh).
+// Compile-time, so that the plain epilogue carries none of them.
+template <bool kSwiglu, bool kAmax, bool kNvfp4>
 __global__ void __launch_bounds__(kThreads, 1)
     nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -402,6 +411,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- epilogue (both CTAs)
         setmaxnreg_inc<kRegsEpi>();
         const int e = warp - kEpiWarp0;    // 0..7
+        float* rcp_tab = reinterpret_cast<float*>(smem + kRcpOff);
+        if constexpr (kNvfp4) {
+            // The reciprocal of every possible block scale of h (the same values
+            // the quantiser uses), shared by the eight epilogue warps.
+            const float s_h = __ldg(p.h_gscale);
+            const int t = (int)threadIdx.x - kEpiWarp0 * 32;
+            if (t < 128) rcp_tab[t] = block_rcp((uint32_t)t, s_h);
+            asm volatile("bar.sync 1, %0;" ::"n"(kEpiWarps * 32) : "memory");
+        }
         const int q = warp & 3;            // TMEM lane quarter this warp may access
         const int h = e >> 2;              // column half of the 256-wide tile
         uint8_t* stg = smem + kEpiOff + e * kEpiWarpBytes;
@@ -452,6 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float* grow = nullptr;
             if (p.gate != nullptr && row < p.M) grow = p.gate + (size_t)segment_of_row(p.seg, row) * p.N;
             bool failed = false;
+            uint32_t hcode[8];       // kNvfp4: this row's 64 values of h as 32 bytes of codes
+            uint32_t hscale = 0u;    // kNvfp4: its four block-scale codes
+            const float s_h_reg = kNvfp4 ? __ldg(p.h_gscale) : 0.0f;
 #pragma unroll
             for (int pass = 0; pass < 2; ++pass) {
                 if (pass == 1 && kSwiglu) break;  // 64 output columns per warp: one pass
@@ -482,6 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // g, u = the plain epilogue's values rounded to bf16 (the FC1
                         // output boundary); h = bf16(silu(g) * u) in fp32.
                         const int ng = nt * BN + 64 * h + 32 * cc;  // gate column of the chunk (up: + 128)
+                        float hv[32];  // kNvfp4: the chunk's 32 values of h, bf16-rounded
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             float bg[8], bu[8];
@@ -521,9 +543,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     if (kAmax && row < p.M) omax = fmaxf(omax, fabsf(o[2 * i + k]));
                                 }
                             }
-                            *reinterpret_cast<uint4*>(buf + swz64(lane, j)) =
-                                make_uint4(cvt_bf16x2(f2(o[0], o[1])), cvt_bf16x2(f2(o[2], o[3])),
-                                           cvt_bf16x2(f2(o[4], o[5])), cvt_bf16x2(f2(o[6], o[7])));
+                            const uint32_t hw[4] = {cvt_bf16x2(f2(o[0], o[1])), cvt_bf16x2(f2(o[2], o[3])),
+                                                    cvt_bf16x2(f2(o[4], o[5])), cvt_bf16x2(f2(o[6], o[7]))};
+                            if constexpr (kNvfp4) {
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    hv[8 * j + 2 * i] = __uint_as_float(hw[i] << 16);
+                                    hv[8 * j + 2 * i + 1] = __uint_as_float(hw[i] & 0xFFFF0000u);
+                                }
+                            } else {
+                                *reinterpret_cast<uint4*>(buf + swz64(lane, j)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                            }
+                        }
+                        if constexpr (kNvfp4) {
+                            // Two 16-value blocks of this row: block scale, codes.
+#pragma unroll
+                            for (int b = 0; b < 2; ++b) {
+                                float bmax = 0.0f;
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(hv[16 * b + i]));
+                                const uint32_t S = block_scale_code(bmax, s_h_reg);
+                                const uint64_t r2 = f2(rcp_tab[S & 127u], rcp_tab[S & 127u]);
+                                float qv[16];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    unf2(mul2(f2(hv[16 * b + 2 * i], hv[16 * b + 2 * i + 1]), r2), qv[2 * i], qv[2 * i + 1]);
+                                hcode[4 * cc + 2 * b] = e2m1x8(reinterpret_cast<const float(&)[8]>(qv[0]));
+                                hcode[4 * cc + 2 * b + 1] = e2m1x8(reinterpret_cast<const float(&)[8]>(qv[8]));
+                                hscale |= S << (8 * (2 * cc + b));
+                            }
+                            continue;
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
@@ -580,6 +629,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (lane == 0) bulk_commit();
+            }
+            if constexpr (kNvfp4) {
+                // Row `row` of h, columns [128 nt + 64 h, +64): 32 bytes of codes and
+                // one 4-byte word of block scales (scale group 2 nt + h) in the
+                // 128x4-tiled layout; rows past M (up to the 128-row padding the
+                // scale layout has) get zero scales and no codes.
+                const int hcol = nt * (BN / 2) + 64 * h;
+                if (row < p.M) {
+                    uint8_t* dst = p.h_codes + (size_t)row * (size_t)(p.N / 4) + hcol / 2;
+                    asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst),
+                                 "r"(hcode[0]), "r"(hcode[1]), "r"(hcode[2]), "r"(hcode[3]), "r"(hcode[4]),
+                                 "r"(hcode[5]), "r"(hcode[6]), "r"(hcode[7])
+                                 : "memory");
+                }
+                if (row < p.m_tiles * BM) {  // the odd CTA of a last pair has no rows in the layout
+                    const size_t soff = ((size_t)(row >> 7) * (size_t)p.h_kb4 + (size_t)(hcol >> 6)) * 512u +
+                                        (size_t)((row & 31) << 4) + (size_t)(((row >> 5) & 3) << 2);
+                    *reinterpret_cast<uint32_t*>(p.h_sf + soff) = row < p.M ? hscale : 0u;
+                }
             }
             if (failed) {
                 if (lane == 0) set_abort();
@@ -676,7 +744,7 @@ static int max_pairs_current_device()
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel<false, false>, &cfg) != cudaSuccess || n <= 0)
+        if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel<false, false, false>, &cfg) != cudaSuccess || n <= 0)
             n = sm_count_current_device() / 2;
         cache[dev] = n;
     }
@@ -701,9 +769,13 @@ static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t 
                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !make_map_2d(&tmSFB, CU_TENSOR_MAP_DATA_TYPE_UINT8, job.w_sf, 256, sfb_rows, 256, 256, kSfBox / 256,
                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !make_map_2d(&tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, job.out, out_cols, (uint64_t)job.M, out_cols * 2, 32,
-                     32, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map_2d(&tmR, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, job.resid ? job.resid : job.out, (uint64_t)job.N,
+        // (NVFP4 output of h: no bf16 output is stored; the map spans the codes
+        // buffer only to be valid)
+        !make_map_2d(&tmOut, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, job.h_codes ? (const void*)job.h_codes : job.out,
+                     job.h_codes ? (uint64_t)job.N / 8 : out_cols, (uint64_t)job.M,
+                     job.h_codes ? (uint64_t)job.N / 4 : out_cols * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_map_2d(&tmR, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     job.resid ? job.resid : (job.out ? job.out : (const void*)job.h_codes), (uint64_t)job.N,
                      (uint64_t)job.M, (uint64_t)job.N * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
 
@@ -726,9 +798,16 @@ static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t 
     p.wait_ns = job.wait_limit_ns;
     p.stall = stall;
     p.amax_out = job.amax_out;
+    p.h_codes = job.h_codes;
+    p.h_sf = job.h_sf;
+    p.h_gscale = job.h_gscale;
+    p.h_kb4 = (int)(job.N / 128);
 
-    auto kernel = job.swiglu ? (job.amax_out ? nvfp4_gemm_kernel<true, true> : nvfp4_gemm_kernel<true, false>)
-                             : (job.amax_out ? nvfp4_gemm_kernel<false, true> : nvfp4_gemm_kernel<false, false>);
+    auto kernel = job.h_codes != nullptr
+                      ? nvfp4_gemm_kernel<true, false, true>
+                      : job.swiglu ? (job.amax_out ? nvfp4_gemm_kernel<true, true, false> : nvfp4_gemm_kernel<true, false, false>)
+                                   : (job.amax_out ? nvfp4_gemm_kernel<false, true, false>
+                                                   : nvfp4_gemm_kernel<false, false, false>);
     const cudaError_t attr_err = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), (int)kSmemBytes);
     if (attr_err != cudaSuccess) return attr_err;
 

@@ -59,6 +59,11 @@ struct GemmJob {
     uint64_t wait_limit_ns;
     bool swiglu;             // SwiGLU epilogue (N % 256 == 0, no gate/residual)
     float* amax_out;         // zeroed by the caller; receives max |out| (or null)
+    // SwiGLU with h written as NVFP4 (codes [M][N/4], block scales of h) under
+    // the given global scale of h; null for a bf16 output
+    uint8_t* h_codes;
+    uint8_t* h_sf;
+    const float* h_gscale;
 };
 
 cudaError_t launch_gemm(const GemmJob& job, cudaStream_t s);

@@ -23,6 +23,7 @@
 
 #include "h3fp4_internal.h"
 #include "ptx_sm103.cuh"
+#include "nvfp4_encode.cuh"
 
 namespace h3fp4 {
 namespace {
@@ -47,50 +48,6 @@ struct QuantParams {
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Eight fp32 values -> eight E2M1 codes in one word, value 2i in bits 8i..8i+3
-// and value 2i+1 in bits 8i+4..8i+7 (RN, saturating to +-6, sign kept).
-__device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8])
-{
-    uint32_t r;
-    asm("{\n\t.reg .b8 t0, t1, t2, t3;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
-        "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
-        "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
-        : "=r"(r)
-        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
-    return r;
-}
-
-// E4M3 code (sign clear) -> fp32 through the hardware E4M3 -> f16 conversion
-// (every E4M3 value is exact in f16, and f16 -> f32 is exact).
-__device__ __forceinline__ float e4m3_value(uint32_t code)
-{
-    float f;
-    asm("{\n\t.reg .b16 c, lo, hi;\n\t.reg .b32 h2;\n\t"
-        "cvt.u16.u32 c, %1;\n\t"
-        "cvt.rn.f16x2.e4m3x2 h2, c;\n\t"
-        "mov.b32 {lo, hi}, h2;\n\t"
-        "cvt.f32.f16 %0, lo;\n\t}"
-        : "=f"(f)
-        : "r"(code));
-    return f;
-}
-
-// RN(b / 6) for b >= 0 a bf16 value (a block maximum), without a division:
-// q = RN(b * RN(1/6)), the remainder b - 6q is exact in one fma, and one more
-// fma applies the correction step of Markstein's FMA-based division.  Equal to
-// the IEEE quotient for every non-negative bf16 value, subnormal quotients
-// included (checked exhaustively).
-__device__ __forceinline__ float div6_bf16(float b)
-{
-    const float c = __uint_as_float(0x3E2AAAABu);  // RN(1/6)
-    const float q = __fmul_rn(b, c);
-    const float r = __fmaf_rn(-q, 6.0f, b);
-    return __fmaf_rn(r, c, q);
-}
 
 // Sixteen bf16 values = 32 bytes: one 256-bit load when the row pointer is
 // 32-byte aligned, two 128-bit loads otherwise.
@@ -270,8 +227,7 @@ __global__ void __launch_bounds__(kThreads, 10) pack_kernel(QuantParams p)
     // conversion never yields the NaN code 0x7F): one table per CTA instead of
     // a multiply and an IEEE reciprocal per block.
     for (int c = threadIdx.x; c < 128; c += kThreads) {
-        const float eff = __fmul_rn(e4m3_value((uint32_t)c), s_g);
-        rcp_tab[c] = (eff == 0.0f || c == 0x7F) ? 0.0f : fminf(__frcp_rn(eff), FLT_MAX);
+        rcp_tab[c] = block_rcp((uint32_t)c, s_g);
     }
     __syncthreads();
 
@@ -312,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 10) pack_kernel(QuantParams p)
             float bmax = 0.0f;
 #pragma unroll
             for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, fabsf(f[j]));
-            const uint32_t S = cvt_e4m3(__fdiv_rn(div6_bf16(bmax), s_g));
+            const uint32_t S = block_scale_code(bmax, s_g);
             const float rcp = rcp_tab[S & 127u];
             const uint64_t rcp2 = f2(rcp, rcp);
             float q[16];
@@ -357,7 +313,33 @@ __global__ void gscale_from_amax_kernel(const float* amax, float* gscale)
     *gscale = (a == 0.0f) ? 1.0f : __fdiv_rn(a, 2688.0f);
 }
 
-QuantParams make_params(const QuantJob& job, dim3* grid)
+// Resident CTAs per SM of each pass (occupancy of its slowest variant),
+// cached once per process (every accepted device is sm_103).
+int amax_ctas_per_sm()
+{
+    static const int n = [] {
+        int a = 0, b = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, amax_kernel<true, true>, kThreads, 0);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, amax_kernel<true, false>, kThreads, 0);
+        return max(1, min(a, b));
+    }();
+    return n;
+}
+
+int pack_ctas_per_sm()
+{
+    static const int n = [] {
+        int a = 0, b = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, pack_kernel<true, true>, kThreads, 0);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, pack_kernel<true, false>, kThreads, 0);
+        return max(1, min(a, b));
+    }();
+    return n;
+}
+
+// Parameters and grid of one pass: one full wave of `per_sm` resident CTAs
+// per SM, each walking a contiguous range of rows (no half-empty second wave).
+QuantParams make_params(const QuantJob& job, int per_sm, dim3* grid)
 {
     QuantParams p{};
     p.x = static_cast<const uint16_t*>(job.x);
@@ -374,15 +356,6 @@ QuantParams make_params(const QuantJob& job, dim3* grid)
     p.partials = job.partials;
 
     const int col_ctas = (int)((job.K / 16 + kThreads - 1) / kThreads);
-    // One full wave of resident CTAs (the slowest variant's occupancy), each
-    // walking a contiguous range of rows: no half-empty second wave.
-    // (thread-safe one-time initialisation; every accepted device is sm_103)
-    static const int per_sm = [] {
-        int a = 0, b = 0;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, pack_kernel<true, true>, kThreads, 0);
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, amax_kernel<true, true>, kThreads, 0);
-        return max(1, min(a, b));
-    }();
     const int target = sm_count_current_device() * per_sm;
     int row_groups = (target + col_ctas - 1) / col_ctas;
     row_groups = max(1, min(row_groups, kMaxPartials / col_ctas));
@@ -436,21 +409,25 @@ cudaError_t launch_pack_t(const QuantParams& p, dim3 grid, bool wide, cudaStream
 
 cudaError_t launch_quantize(const QuantJob& job, cudaStream_t s)
 {
-    dim3 grid;
-    const QuantParams p = make_params(job, &grid);
+    // Each pass gets its own one-wave grid; the pack pass reduces the partials
+    // of the amax pass's grid.
+    dim3 agrid, pgrid;
+    const QuantParams pa = make_params(job, amax_ctas_per_sm(), &agrid);
+    QuantParams pp = make_params(job, pack_ctas_per_sm(), &pgrid);
+    pp.nparts = pa.nparts;
     const bool mod = job.shift != nullptr;
     const bool wide = wide_ok(job.x);
     if (!job.gscale_given) {
-        const cudaError_t e = mod ? launch_amax_t<true>(p, grid, wide, s) : launch_amax_t<false>(p, grid, wide, s);
+        const cudaError_t e = mod ? launch_amax_t<true>(pa, agrid, wide, s) : launch_amax_t<false>(pa, agrid, wide, s);
         if (e != cudaSuccess) return e;
     }
-    return mod ? launch_pack_t<true>(p, grid, wide, s) : launch_pack_t<false>(p, grid, wide, s);
+    return mod ? launch_pack_t<true>(pp, pgrid, wide, s) : launch_pack_t<false>(pp, pgrid, wide, s);
 }
 
 cudaError_t launch_amax(const QuantJob& job, float* amax_out, cudaStream_t s)
 {
     dim3 grid;
-    const QuantParams p = make_params(job, &grid);
+    const QuantParams p = make_params(job, amax_ctas_per_sm(), &grid);
     const cudaError_t e = job.shift != nullptr ? launch_amax_t<true>(p, grid, wide_ok(job.x), s)
                                                : launch_amax_t<false>(p, grid, wide_ok(job.x), s);
     if (e != cudaSuccess) return e;

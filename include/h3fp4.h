@@ -179,6 +179,30 @@ H3FP4_API h3fp4_status h3fp4_linear(const void* x, const void* a_sf, const float
                           const void* bias_bf16, const void* resid_bf16, void* out_bf16,
                           int flags, void* ws, cudaStream_t stream);
 
+/* FC1 with the SwiGLU producer writing h straight to NVFP4: the FC2 operand
+ * leaves the FC1 epilogue as codes and block scales, so h is never stored in
+ * bf16 and FC2 needs no quantisation pass ("H3 Runtime Current State", "Owned
+ * Performance Kernels": the exact SwiGLU-to-FC2 NVFP4 producer fusion that
+ * emits tensor scale/QDATA/SFA).
+ *   Arguments as in h3fp4_linear with H3FP4_EPI_SWIGLU (N % 256 == 0, the
+ *   weight's [gate 128 | up 128] row groups); flags: H3FP4_PROLOGUE_MOD,
+ *   H3FP4_EPI_BIAS, H3FP4_GSCALE_GIVEN, H3FP4_A_PREQUANT (the activation x).
+ *   h_gscale: device fp32 > 0, the global scale of h, an INPUT (for instance
+ *   h3fp4_gscale_from_amax of the EPI_AMAX output of an earlier call, or a
+ *   calibrated scale).  h_codes [M][N/4] bytes and h_sf
+ *   (h3fp4_sf_bytes(M, N/2)) receive exactly what
+ *   h3fp4_quantize_act(h, ..., H3FP4_GSCALE_GIVEN with *h_gscale) would write
+ *   for the bf16 h that h3fp4_linear's SwiGLU epilogue stores; a following
+ *   h3fp4_linear with H3FP4_A_PREQUANT (a_sf = h_sf, a_gscale = h_gscale)
+ *   consumes them.  h_codes may not alias x or the weights. */
+H3FP4_API h3fp4_status h3fp4_linear_swiglu_nvfp4(const void* x, const void* a_sf, const float* a_gscale,
+                                    int64_t M, int64_t N, int64_t K,
+                                    const void* w_codes, const void* w_sf, const float* w_gscale,
+                                    const float* shift, const float* scale,
+                                    const int64_t* seg_off, int nseg, const void* bias_bf16,
+                                    const float* h_gscale, void* h_codes, void* h_sf,
+                                    int flags, void* ws, cudaStream_t stream);
+
 /* Quantise an activation exactly like h3fp4_quantize_act, but without a
  * workspace and without allocating anything, for callers that are handed only
  * their input and output buffers: for example a plugin whose host application

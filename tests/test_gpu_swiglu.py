@@ -182,3 +182,51 @@ def test_out_amax_with_gate_residual_and_segments():
     out = case.run(out_amax=True)
     torch.cuda.synchronize()
     _check_amax(out, A.h3fp4_ws_out_amax(case.ws).clone())
+
+
+def _nvfp4_out_case(orc, M, N, K, check_oracle=True):
+    """FC1 SwiGLU writing h as NVFP4 under the scale of its own amax, against
+    the quantiser (GPU and oracle) applied to the bf16 h of the plain SwiGLU
+    epilogue, and FC2 on those codes against FC2 on h with the same scale."""
+    import audio_dit_gb300 as A
+    from _gpu_helpers import check_guards, dev_bf16, guarded_nvfp4
+    d = W.swiglu_fc1_inputs(M, N, K)
+    case, _, h, _, amax_h = _run_pair(d)
+    gs = torch.empty(1, dtype=torch.float32, device="cuda")
+    A.h3fp4_gscale_from_amax(amax_h, gs)
+    gq = guarded_nvfp4(M, N // 2)
+    codes, sf = gq[0].t, gq[1].t
+    A.h3fp4_linear_swiglu_nvfp4(case.x, *case.wq, codes, sf, gs, case.ws, shift=case.shift, scale=case.scale,
+                                bias=case.bias)
+    A.h3fp4_check(case.ws)
+    check_guards(gq[:2], "h NVFP4")
+    case.check_guards()
+    hb = host_u16(h)
+    got = (codes.cpu().numpy(), sf.cpu().numpy(), float(gs.cpu()[0]))
+    assert_quant_equal(got, gpu_quantize(hb, gscale=got[2]), "h NVFP4 vs GPU quantiser")
+    if check_oracle:
+        assert_quant_equal(got, orc.quantize(hb, gscale=got[2]), "h NVFP4 vs oracle quantiser")
+    # FC2 on the emitted codes == FC2 on h with the same global scale
+    rng = np.random.default_rng(M + N)
+    N2 = 256
+    w2 = W.to_bf16_bits(rng.standard_normal((N2, N // 2), dtype=np.float32) * np.float32(0.01))
+    wq2 = A.alloc_nvfp4(N2, N // 2)
+    ws2 = A.alloc_workspace(M, N2, N // 2, 0)
+    A.h3fp4_quantize_weight(dev_bf16(w2), *wq2, ws2)
+    o_codes = torch.empty((M, N2), dtype=torch.bfloat16, device="cuda")
+    o_h = torch.empty_like(o_codes)
+    A.h3fp4_linear(codes, *wq2, o_codes, ws2, a_sf=sf, a_gscale=gs)
+    A.h3fp4_linear(h, *wq2, o_h, ws2, a_gscale=gs, gscale_given=True)
+    A.h3fp4_check(ws2)
+    assert torch.equal(o_codes.view(torch.int16), o_h.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 512, 512), (1000, 1024, 3072), (129, 256, 64), (385, 768, 320)])
+def test_swiglu_nvfp4_output(orc, M, N, K):
+    _nvfp4_out_case(orc, M, N, K)
+
+
+def test_swiglu_nvfp4_output_full_size(orc):
+    """FC1 at full size (X [32768, 3072], W [24576, 3072]): h [32768, 12288]
+    emitted as NVFP4 equals the quantiser's bytes for the bf16 h."""
+    _nvfp4_out_case(orc, 32768, 24576, 3072)
