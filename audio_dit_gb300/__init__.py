@@ -21,7 +21,7 @@ __all__ = [
     "EPI_SWIGLU", "EPI_AMAX", "h3fp4_ws_out_amax",
     "MAX_SEGMENTS", "library_path", "load_library", "h3fp4_codes_bytes", "h3fp4_sf_bytes",
     "h3fp4_workspace_bytes", "h3fp4_quantize_weight", "h3fp4_quantize_act", "h3fp4_linear",
-    "h3fp4_check", "h3fp4_act_amax", "h3fp4_gscale_from_amax", "h3fp4_selftest_timeout", "h3fp4_measure_fp4_peak", "h3fp4_measure_fp4_pair_peak", "h3fp4_quantize_act_noalloc",
+    "h3fp4_check", "h3fp4_act_amax", "h3fp4_gscale_from_amax", "h3fp4_selftest_timeout", "h3fp4_measure_fp4_peak", "h3fp4_measure_fp4_pair_peak", "h3fp4_measure_fp4_form", "MMA_FORMS", "h3fp4_quantize_act_noalloc",
     "h3fp4_linear_swiglu_nvfp4", "h3fp4_set_wait_limit_ns", "h3fp4_status_string", "alloc_nvfp4", "alloc_workspace",
 ]
 
@@ -74,6 +74,7 @@ def load_library():
         "h3fp4_selftest_timeout": (i32, [vp, C.c_uint64, vp]),
         "h3fp4_measure_fp4_peak": (i32, [i32, vp, vp]),
         "h3fp4_measure_fp4_pair_peak": (i32, [i32, vp, vp]),
+        "h3fp4_measure_fp4_form": (i32, [i32, i32, vp, vp]),
         "h3fp4_quantize_act_noalloc": (i32, [vp, i64, i64, vp, vp, vp, i32, vp, vp, vp, i32, vp]),
         "h3fp4_check": (i32, [vp, vp]),
         "h3fp4_set_wait_limit_ns": (None, [C.c_uint64]),
@@ -287,6 +288,19 @@ def h3fp4_measure_fp4_pair_peak(ws: torch.Tensor, iters: int = 20000) -> float:
     out = C.c_float(0.0)
     _check(load_library().h3fp4_measure_fp4_pair_peak(int(iters), C.byref(out), _ptr(ws, "ws", torch.uint8)),
            "h3fp4_measure_fp4_pair_peak")
+    return float(out.value)
+
+
+MMA_FORMS = {0: "cta_group::1 M=128 N=256 K=64, A smem", 1: "cta_group::2 M=256 N=256 K=64, A smem",
+             2: "cta_group::1, A TMEM", 3: "cta_group::2, A TMEM", 4: "cta_group::1, 2 x N=128 sharing A",
+             5: "cta_group::1, 2 x N=128, collector::a fill/lastuse", 6: "cta_group::2, 2 x N=128 sharing A"}
+
+
+def h3fp4_measure_fp4_form(ws: torch.Tensor, form: int, iters: int = 20000) -> float:
+    """Measured ceiling (TFLOP/s) of one kind::mxf4nvf4 MMA form (MMA_FORMS; synchronous)."""
+    out = C.c_float(0.0)
+    _check(load_library().h3fp4_measure_fp4_form(int(form), int(iters), C.byref(out), _ptr(ws, "ws", torch.uint8)),
+           "h3fp4_measure_fp4_form")
     return float(out.value)
 
 

@@ -417,6 +417,16 @@ h3fp4_status h3fp4_measure_fp4_pair_peak(int iters, float* tflops, void* ws)
         measure_fp4_pair_peak(iters, reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + kWsStatus), tflops));
 }
 
+h3fp4_status h3fp4_measure_fp4_form(int form, int iters, float* tflops, void* ws)
+{
+    if (!tflops || !ws || iters < 1 || form < H3FP4_MMA_SINGLE || form > H3FP4_MMA_PAIR_N128)
+        return H3FP4_ERR_INVALID;
+    h3fp4_status st = check_device();
+    if (st != H3FP4_OK) return st;
+    return from_cuda(measure_fp4_form(form, iters,
+                                      reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + kWsStatus), tflops));
+}
+
 h3fp4_status h3fp4_check(void* ws, cudaStream_t stream)
 {
     if (!ws) return H3FP4_ERR_INVALID;

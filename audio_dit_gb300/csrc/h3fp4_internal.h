@@ -100,4 +100,7 @@ cudaError_t measure_fp4_peak(int iters, unsigned int* status, float* tflops);
 // The same for the paired (cta_group::2) MMA on every 2-CTA cluster.
 cudaError_t measure_fp4_pair_peak(int iters, unsigned int* status, float* tflops);
 
+// The same for any h3fp4_mma_form.
+cudaError_t measure_fp4_form(int form, int iters, unsigned int* status, float* tflops);
+
 }  // namespace h3fp4

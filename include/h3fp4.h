@@ -121,14 +121,21 @@ H3FP4_API size_t h3fp4_sf_bytes(int64_t rows, int64_t K);
 H3FP4_API size_t h3fp4_workspace_bytes(int64_t M, int64_t N, int64_t K, int flags);
 
 /* Quantise a weight W [N, K] bf16 to NVFP4 (offline step; same algorithm as
- * the activations, no prologue).  Writes codes [N][K/2], sf
+ * the activations, no prologue).  Passage: "H3 Blackwell Runtime" README,
+ * "Checkpoints" (pre-quantised NVFP4 weights, not converted at run time);
+ * the format as in h3fp4_quantize_act.  Writes codes [N][K/2], sf
  * (h3fp4_sf_bytes(N, K)) and *w_gscale (device).  ws: h3fp4_workspace_bytes
  * (N, 0, K, 0) bytes. */
 H3FP4_API h3fp4_status h3fp4_quantize_weight(const void* w_bf16, int64_t N, int64_t K,
                                    void* codes, void* sf, float* w_gscale,
                                    void* ws, cudaStream_t stream);
 
-/* Quantise an activation X [M, K] bf16.
+/* Quantise an activation X [M, K] bf16.  Passages: "H3 Runtime Current
+ * State", "Owned Performance Kernels" (scale discovery then pack into
+ * QDATA + swizzled block scales; one full-activation scale; modulation fed
+ * into scale/pack as exact BF16 values) and "H3 Blackwell Runtime Plan",
+ * "Next Performance Plan: Blackwell NVFP4 GEMMs" (signed zero, tie-to-even FP4
+ * rounding, cuBLAS tiled block-scale layout).
  *   shift, scale: fp32 [nseg][K] (device), required with H3FP4_PROLOGUE_MOD.
  *   seg_off: HOST array of nseg + 1 row offsets, seg_off[0] = 0,
  *            non-decreasing, seg_off[nseg] = M; NULL means one segment.
@@ -143,6 +150,11 @@ H3FP4_API h3fp4_status h3fp4_quantize_act(const void* x_bf16, int64_t M, int64_t
                                 int flags, void* ws, cudaStream_t stream);
 
 /* The NVFP4 linear: out[M][N] (bf16) from X and a quantised weight.
+ * Passages: "H3 Runtime Current State", "Owned Performance Kernels" (the
+ * block-scaled NVFP4 GEMM of the four projections, alpha applied before the
+ * BF16 cast, gate/add epilogue; removing intermediate traffic across the
+ * scale/pack/GEMM boundaries) and "Implemented And Validated" (fused
+ * modulation and residual gates over packed video+audio tokens).
  *   x: bf16 [M][K], or codes [M][K/2] with H3FP4_A_PREQUANT (then a_sf and
  *      a_gscale describe it).  With H3FP4_GSCALE_GIVEN a_gscale (device) is
  *      the activation global scale; otherwise it may be NULL and the scale is
@@ -274,6 +286,25 @@ H3FP4_API h3fp4_status h3fp4_measure_fp4_peak(int iters, float* tflops, void* ws
  * default stream).  Writes TFLOP/s to *tflops; ws: any workspace (status word
  * only).  No counterpart in the pages: it measures this GPU. */
 H3FP4_API h3fp4_status h3fp4_measure_fp4_pair_peak(int iters, float* tflops, void* ws);
+
+/* The tcgen05 forms of the NVFP4 block-scaled MMA (kind::mxf4nvf4,
+ * scale_vec::4X: E2M1 operands, 16-element blocks with E4M3 scales -- the only
+ * kind that carries NVFP4) that h3fp4_measure_fp4_form can time. */
+typedef enum {
+    H3FP4_MMA_SINGLE = 0,                 /* cta_group::1, M=128, N=256, K=64, A in shared memory */
+    H3FP4_MMA_PAIR = 1,                   /* cta_group::2, M=256, N=256, K=64 (the GEMM's form)     */
+    H3FP4_MMA_SINGLE_TMEM_A = 2,          /* cta_group::1 with A read from TMEM                     */
+    H3FP4_MMA_PAIR_TMEM_A = 3,            /* cta_group::2 with A read from TMEM                     */
+    H3FP4_MMA_SINGLE_N128 = 4,            /* cta_group::1, two N=128 MMAs per K step sharing A      */
+    H3FP4_MMA_SINGLE_N128_COLLECTOR = 5,  /* the same through .collector::a::fill / ::lastuse       */
+    H3FP4_MMA_PAIR_N128 = 6               /* cta_group::2, two N=128 MMAs per K step sharing A      */
+} h3fp4_mma_form;
+
+/* Measured ceiling (TFLOP/s, synchronous) of one MMA form, issued back to back
+ * by one thread per CTA (or CTA pair) on every SM with operands and scales
+ * resident on chip; flops counted as 2 * 128 * 256 * 64 per CTA per K step.
+ * Entry point for roofline evidence only; no counterpart on the pages. */
+H3FP4_API h3fp4_status h3fp4_measure_fp4_form(int form, int iters, float* tflops, void* ws);
 
 /* Synchronises `stream`, reads and clears the workspace status word.
  * Returns H3FP4_OK, or H3FP4_ERR_TIMEOUT when a kernel gave up early (a
