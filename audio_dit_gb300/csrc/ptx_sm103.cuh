@@ -428,6 +428,22 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b)
     return d;
 }
 
+// The hardware's approximate 2^x and 1/x (PTX ex2.approx.f32, rcp.approx.f32;
+// no .ftz, so subnormal arguments and results keep their values).
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float y;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Two fp32 lanes -> one bf16x2 word (lo in bits 0-15), each rounded to nearest even.
 __device__ __forceinline__ uint32_t cvt_bf16x2(uint64_t v)
 {

@@ -173,7 +173,9 @@ H3FP4_API h3fp4_status h3fp4_quantize_act(const void* x_bf16, int64_t M, int64_t
  * [128 t, 128 t + 128).  With g, u the bf16 outputs the plain epilogue would
  * write for a gate and its up row (the FC1 output boundary),
  *     out[m][128 t + i] = bf16(silu(g) * u),  silu(g) = g / (1 + e^-g),
- * evaluated in fp32 (IEEE divide, CUDA expf); out is [M][N/2].  Not with
+ * evaluated in fp32 from the hardware's approximate 2^x and 1/x in a form that
+ * cannot overflow (within one bf16 step of the exact value for every bf16 g);
+ * out is [M][N/2].  Not with
  * H3FP4_EPI_GATE_RESID.
  *
  * Output amax (H3FP4_EPI_AMAX; "H3 Blackwell Runtime Plan", "Next Performance
