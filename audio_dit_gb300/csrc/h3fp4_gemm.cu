@@ -80,7 +80,6 @@ namespace {
 constexpr int BM = 128;                               // rows of A per CTA (256 per pair)
 constexpr int BN = 256;                               // rows of W per pair tile
 constexpr int BK = 256;                               // K elements per stage
-constexpr int kStages = 5;
 constexpr int kThreads = 512;
 constexpr int kScaleWarp0 = 4;   // warps 4..7: scale warps, lane quarter = warp & 3
 constexpr int kEpiWarp0 = 8;     // warps 8..15: epilogue
@@ -95,19 +94,35 @@ constexpr uint32_t kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;  // 
 constexpr uint32_t kPairTxBytes = 2 * (kABytes + kBBytes);  // both CTAs' code tiles complete on the leader
 constexpr uint32_t kSfBox = 2048;                     // scale-tile TMA box: 8 rows x 256 bytes
 constexpr uint32_t kChunkBytes = 32 * 32 * 2;         // 32 rows x 32 bf16
-constexpr uint32_t kEpiWarpBytes = 2 * kChunkBytes;   // 4096: two staging buffers
-constexpr uint32_t kEpiOff = kStages * kStageBytes;
-constexpr uint32_t kBarOff = kEpiOff + kEpiWarps * kEpiWarpBytes;
-constexpr uint32_t kBarBytes = 8 * (3 * kStages + 3 + kEpiWarps) + 8;  // barriers, TMEM address, abort flag
-constexpr uint32_t kRcpOff = kBarOff + 512;             // kNvfp4: 128 fp32 block reciprocals of h
-constexpr uint32_t kSmemBytes = kRcpOff + 512;
-static_assert(kBarBytes <= 512, "barrier block");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmem = 256;
 constexpr uint32_t kSfTmemPerStage = 48;
-static_assert(kSfTmem + kStages * kSfTmemPerStage <= kTmemCols, "TMEM budget");
-static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kStageBytes % 1024 == 0, "stages must keep the 1024-byte swizzle alignment");
+
+// Ring depth and epilogue staging.  The default plan keeps five stages in
+// flight and two 32x32 staging chunks per epilogue warp, so a gated epilogue
+// loads its second pass's residual only after the first pass's stores have
+// read the chunks.  The wide plan (gated residual epilogue over a short K
+// loop, where that epilogue is longer than a tile's mainloop) gives up one
+// stage for four chunks per warp: the whole tile's residual is loaded ahead
+// of the accumulator, and the epilogue runs in one pass.
+// K stages per tile below which a gated residual epilogue takes the wide plan.
+constexpr int kWideMaxKStages = 24;
+
+template <bool kWide>
+struct Plan {
+    static constexpr int kStages = kWide ? 4 : 5;
+    static constexpr int kChunks = kWide ? 4 : 2;               // staging chunks per epilogue warp
+    static constexpr uint32_t kEpiWarpBytes = kChunks * kChunkBytes;
+    static constexpr uint32_t kEpiOff = kStages * kStageBytes;
+    static constexpr uint32_t kBarOff = kEpiOff + kEpiWarps * kEpiWarpBytes;
+    static constexpr uint32_t kBarBytes = 8 * (3 * kStages + 3 + kEpiWarps) + 8;  // barriers, TMEM address, abort flag
+    static constexpr uint32_t kRcpOff = kBarOff + 512;          // kNvfp4: 128 fp32 block reciprocals of h
+    static constexpr uint32_t kSmemBytes = kRcpOff + 512;
+    static_assert(kBarBytes <= 512, "barrier block");
+    static_assert(kSfTmem + kStages * kSfTmemPerStage <= kTmemCols, "TMEM budget");
+    static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
 static_assert(kSFABytes == kSfBox && kSFBBytes == 2 * kSfBox, "scale tiles move in 2 KB boxes");
 
 // Instruction descriptor, kind::mxf4nvf4: A/B E2M1 (1) in bits 7-9 / 10-12,
@@ -168,8 +183,9 @@ __device__ __forceinline__ float silu_f32(float g)
 // kSwiglu: SwiGLU epilogue (out [M][N/2]); kAmax: track max |out| into p.amax_out;
 // kNvfp4 (with kSwiglu): h is not stored in bf16 but quantised to NVFP4 under the
 // given global scale of h, with the quantiser's arithmetic (nvfp4_encode.cuh).
-// Compile-time, so that the plain epilogue carries none of them.
-template <bool kSwiglu, bool kAmax, bool kNvfp4>
+// Compile-time, so that the plain epilogue carries none of them.  kWide: the
+// wide plan (Plan above; gated residual epilogue only).
+template <bool kSwiglu, bool kAmax, bool kNvfp4, bool kWide>
 __global__ void __launch_bounds__(kThreads, 1)
     nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
@@ -177,6 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const GemmParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
+    static_assert(!kWide || !kSwiglu, "the wide plan is for the gated residual epilogue");
+    using P = Plan<kWide>;
+    constexpr int kStages = P::kStages;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // Swizzled TMA tiles need 1024-byte alignment; refuse to run otherwise.  Both
@@ -191,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Leader's "full": both CTAs' code tiles landed (tx bytes) AND the eight
     // scale warps of the pair stored the stage's scales in TMEM (arrivals), so
     // one wait clears a stage for the MMAs.
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOff);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + P::kBarOff);
     uint64_t* empty = full + kStages;                                // both: the MMAs released the stage
     uint64_t* sf_full = empty + kStages;                             // both: this CTA's scale tiles landed
     uint64_t* acc_full = sf_full + kStages;                          // both: accumulator complete
@@ -423,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------------- epilogue (both CTAs)
         setmaxnreg_inc<kRegsEpi>();
         const int e = warp - kEpiWarp0;    // 0..7
-        float* rcp_tab = reinterpret_cast<float*>(smem + kRcpOff);
+        float* rcp_tab = reinterpret_cast<float*>(smem + P::kRcpOff);
         if constexpr (kNvfp4) {
             // The reciprocal of every possible block scale of h (the same values
             // the quantiser uses), shared by the eight epilogue warps.
@@ -434,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int q = warp & 3;            // TMEM lane quarter this warp may access
         const int h = e >> 2;              // column half of the 256-wide tile
-        uint8_t* stg = smem + kEpiOff + e * kEpiWarpBytes;
+        uint8_t* stg = smem + P::kEpiOff + e * P::kEpiWarpBytes;
         const float alpha = __fmul_rn(__ldg(p.a_gscale), __ldg(p.w_gscale));
         const uint64_t alpha2 = f2(alpha, alpha);
         uint32_t acc_phase = 0, r_phase = 0;
@@ -446,14 +465,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (blockIdx.x & 1 is the CTA's rank in its pair)
             const int m0 = (2 * mp + (int)(blockIdx.x & 1u)) * BM + 32 * q;  // first row of this warp
             const int nc0 = nt * BN + 128 * h;                                 // first column of this warp
-            // Two passes of two 32x32 chunks through the warp's two staging
-            // buffers; the residual chunks of a pass are TMA-loaded into them
-            // first (pass 0 ahead of the accumulator).
+            // Two passes of two 32x32 chunks through the warp's staging chunks;
+            // the residual chunks of a pass are TMA-loaded into them first (pass 0
+            // ahead of the accumulator; with the wide plan all four chunks).
             if (lane == 0) bulk_wait_read_all();  // staging buffers free again
             __syncwarp();
             if (p.has_resid && lane == 0) {
-                mbar_arrive_expect_tx(&rbar[e], 2 * kChunkBytes);
-                for (int c = 0; c < 2; ++c) tma_load_2d(stg + c * kChunkBytes, &tmR, &rbar[e], nc0 + 32 * c, m0);
+                mbar_arrive_expect_tx(&rbar[e], P::kChunks * kChunkBytes);
+                for (int c = 0; c < P::kChunks; ++c)
+                    tma_load_2d(stg + c * kChunkBytes, &tmR, &rbar[e], nc0 + 32 * c, m0);
             }
             r_pending = p.has_resid != 0;
             bool ok = mbar_wait(acc_full, acc_phase, p.wait_ns, p.status, kStatusTimeoutEpilogue);
@@ -488,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int pass = 0; pass < 2; ++pass) {
                 if (pass == 1 && kSwiglu) break;  // 64 output columns per warp: one pass
-                if (pass == 1) {
+                if (pass == 1 && !kWide) {
                     if (lane == 0) bulk_wait_read_all();  // pass 0's stores have read the buffers
                     __syncwarp();
                     if (p.has_resid && lane == 0) {
@@ -498,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     r_pending = p.has_resid != 0;
                 }
-                if (p.has_resid) {
+                if (p.has_resid && (pass == 0 || !kWide)) {
                     ok = mbar_wait(&rbar[e], r_phase, p.wait_ns, p.status, kStatusTimeoutEpilogue);
                     if (!__all_sync(0xffffffffu, ok)) {
                         failed = true;
@@ -510,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     const int c = 2 * pass + cc;
-                    uint8_t* buf = stg + cc * kChunkBytes;
+                    uint8_t* buf = stg + (kWide ? c : cc) * kChunkBytes;
                     if constexpr (kSwiglu) {
                         // g, u = the plain epilogue's values rounded to bf16 (the FC1
                         // output boundary); h = bf16(silu(g) * u) in fp32.
@@ -752,11 +772,14 @@ static int max_pairs_current_device()
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3(2 * (unsigned)sm_count_current_device());
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.dynamicSmemBytes = Plan<false>::kSmemBytes;  // one CTA per SM with either plan
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel<false, false, false>, &cfg) != cudaSuccess || n <= 0)
+        const void* probe = reinterpret_cast<const void*>(nvfp4_gemm_kernel<false, false, false, false>);
+        if (ensure_dynamic_smem(probe, (int)Plan<false>::kSmemBytes) != cudaSuccess ||
+            cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel<false, false, false, false>, &cfg) != cudaSuccess ||
+            n <= 0)
             n = sm_count_current_device() / 2;
         cache[dev] = n;
     }
@@ -815,12 +838,17 @@ static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t 
     p.h_gscale = job.h_gscale;
     p.h_kb4 = (int)(job.N / 128);
 
-    auto kernel = job.h_codes != nullptr
-                      ? nvfp4_gemm_kernel<true, false, true>
-                      : job.swiglu ? (job.amax_out ? nvfp4_gemm_kernel<true, true, false> : nvfp4_gemm_kernel<true, false, false>)
-                                   : (job.amax_out ? nvfp4_gemm_kernel<false, true, false>
-                                                   : nvfp4_gemm_kernel<false, false, false>);
-    const cudaError_t attr_err = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), (int)kSmemBytes);
+    // The wide plan where a tile's gated epilogue outlasts its mainloop (short K).
+    const bool wide = p.has_resid && !job.swiglu && job.h_codes == nullptr && p.k_stages < kWideMaxKStages;
+    auto kernel = job.h_codes != nullptr ? nvfp4_gemm_kernel<true, false, true, false>
+                  : job.swiglu ? (job.amax_out ? nvfp4_gemm_kernel<true, true, false, false>
+                                               : nvfp4_gemm_kernel<true, false, false, false>)
+                  : wide ? (job.amax_out ? nvfp4_gemm_kernel<false, true, false, true>
+                                         : nvfp4_gemm_kernel<false, false, false, true>)
+                         : (job.amax_out ? nvfp4_gemm_kernel<false, true, false, false>
+                                         : nvfp4_gemm_kernel<false, false, false, false>);
+    const uint32_t smem_bytes = wide ? Plan<true>::kSmemBytes : Plan<false>::kSmemBytes;
+    const cudaError_t attr_err = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), (int)smem_bytes);
     if (attr_err != cudaSuccess) return attr_err;
 
     const int tiles = p.pair_m_tiles * p.n_tiles;
@@ -837,7 +865,7 @@ static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = dim3(2 * (unsigned)pairs);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
