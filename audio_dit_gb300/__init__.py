@@ -18,7 +18,7 @@ import torch
 
 __all__ = [
     "H3FP4Error", "PROLOGUE_MOD", "EPI_BIAS", "EPI_GATE_RESID", "GSCALE_GIVEN", "A_PREQUANT",
-    "EPI_SWIGLU", "EPI_AMAX", "h3fp4_ws_out_amax",
+    "EPI_SWIGLU", "EPI_AMAX", "FUSED_QUANT", "h3fp4_ws_out_amax", "h3fp4_selftest_pack_timeout",
     "MAX_SEGMENTS", "library_path", "load_library", "h3fp4_codes_bytes", "h3fp4_sf_bytes",
     "h3fp4_workspace_bytes", "h3fp4_quantize_weight", "h3fp4_quantize_act", "h3fp4_linear",
     "h3fp4_check", "h3fp4_act_amax", "h3fp4_gscale_from_amax", "h3fp4_selftest_timeout", "h3fp4_measure_fp4_peak", "h3fp4_measure_fp4_pair_peak", "h3fp4_measure_fp4_form", "MMA_FORMS", "h3fp4_quantize_act_noalloc",
@@ -32,6 +32,7 @@ GSCALE_GIVEN = 16
 A_PREQUANT = 32
 EPI_SWIGLU = 64
 EPI_AMAX = 128
+FUSED_QUANT = 256
 MAX_SEGMENTS = 8
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -72,6 +73,7 @@ def load_library():
         "h3fp4_gscale_from_amax": (i32, [vp, vp, vp]),
         "h3fp4_ws_out_amax": (vp, [vp]),
         "h3fp4_selftest_timeout": (i32, [vp, C.c_uint64, vp]),
+        "h3fp4_selftest_pack_timeout": (i32, [vp, vp, vp, C.c_uint64, vp]),
         "h3fp4_measure_fp4_peak": (i32, [i32, vp, vp]),
         "h3fp4_measure_fp4_pair_peak": (i32, [i32, vp, vp]),
         "h3fp4_measure_fp4_form": (i32, [i32, i32, vp, vp]),
@@ -174,13 +176,14 @@ def h3fp4_linear(x: torch.Tensor, w_codes: torch.Tensor, w_sf: torch.Tensor, w_g
                  gate: Optional[torch.Tensor] = None, resid: Optional[torch.Tensor] = None,
                  bias: Optional[torch.Tensor] = None, seg_off: Optional[Sequence[int]] = None,
                  gscale_given: bool = False, swiglu: bool = False, out_amax: bool = False,
-                 stream=None) -> None:
+                 fused: bool = False, stream=None) -> None:
     """out = [R + g*](alpha * NVFP4(prologue(x)) . W^T [+ b]).
 
     ``x`` is bf16 [M, K]; or uint8 codes [M, K/2] together with ``a_sf`` and
     ``a_gscale`` (pre-quantised activation).  ``swiglu``: out is [M, N/2] =
     bf16(silu(g) * u) over the weight's [gate 128 | up 128] row groups.
     ``out_amax``: also leave max|out| at :func:`h3fp4_ws_out_amax` (ws).
+    ``fused``: the GEMM kernel quantises x itself (H3FP4_FUSED_QUANT).
     """
     prequant = x.dtype == torch.uint8
     M = x.shape[0]
@@ -189,7 +192,7 @@ def h3fp4_linear(x: torch.Tensor, w_codes: torch.Tensor, w_sf: torch.Tensor, w_g
     flags = ((A_PREQUANT if prequant else 0) | (PROLOGUE_MOD if shift is not None else 0)
              | (EPI_BIAS if bias is not None else 0) | (EPI_GATE_RESID if gate is not None else 0)
              | (GSCALE_GIVEN if gscale_given else 0) | (EPI_SWIGLU if swiglu else 0)
-             | (EPI_AMAX if out_amax else 0))
+             | (EPI_AMAX if out_amax else 0) | (FUSED_QUANT if fused else 0))
     sp, nseg, _keep = _segs(seg_off)
     _check(load_library().h3fp4_linear(
         _ptr(x, "x"), _ptr(a_sf, "a_sf", torch.uint8), _ptr(a_gscale, "a_gscale", torch.float32), M, N, K,
@@ -273,6 +276,14 @@ def h3fp4_gscale_from_amax(amax: torch.Tensor, gscale: torch.Tensor, stream=None
 def h3fp4_selftest_timeout(ws: torch.Tensor, limit_ns: int, stream=None) -> None:
     _check(load_library().h3fp4_selftest_timeout(_ptr(ws, "ws", torch.uint8), int(limit_ns), _stream(stream)),
            "h3fp4_selftest_timeout")
+
+
+def h3fp4_selftest_pack_timeout(x: torch.Tensor, a_gscale: torch.Tensor, ws: torch.Tensor, limit_ns: int,
+                                stream=None) -> None:
+    _check(load_library().h3fp4_selftest_pack_timeout(_ptr(x, "x", torch.bfloat16),
+                                                      _ptr(a_gscale, "a_gscale", torch.float32),
+                                                      _ptr(ws, "ws", torch.uint8), int(limit_ns), _stream(stream)),
+           "h3fp4_selftest_pack_timeout")
 
 
 def h3fp4_measure_fp4_peak(ws: torch.Tensor, iters: int = 20000) -> float:

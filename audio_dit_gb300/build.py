@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libh3fp4.so")
 SOURCES = ["h3fp4_api.cu", "h3fp4_quant.cu", "h3fp4_gemm.cu", "h3fp4_peak.cu", "h3fp4_noalloc.cu"]
-HEADERS = ["h3fp4_internal.h", "ptx_sm103.cuh", "nvfp4_encode.cuh"]
+HEADERS = ["h3fp4_internal.h", "ptx_sm103.cuh", "nvfp4_encode.cuh", "act_prologue.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -121,7 +121,9 @@ size_t h3fp4_workspace_bytes(int64_t M, int64_t N, int64_t K, int flags)
 {
     (void)N;
     size_t bytes = kWsActCodes;
-    if (!(flags & H3FP4_A_PREQUANT)) bytes += round256(h3fp4_codes_bytes(M, K)) + round256(h3fp4_sf_bytes(M, K));
+    if (!(flags & H3FP4_A_PREQUANT))
+        bytes += round256(h3fp4_codes_bytes(M, K)) + round256(h3fp4_sf_bytes(M, K)) +
+                 round256(4 * pack_flag_words(M, K));
     return bytes;
 }
 
@@ -188,7 +190,7 @@ h3fp4_status h3fp4_linear(const void* x, const void* a_sf, const float* a_gscale
     if (st != H3FP4_OK) return st;
     if (N < 8 || N % 8 != 0 || N > (int64_t)INT32_MAX) return H3FP4_ERR_SHAPE;
     const int known = H3FP4_PROLOGUE_MOD | H3FP4_EPI_BIAS | H3FP4_EPI_GATE_RESID | H3FP4_GSCALE_GIVEN |
-                      H3FP4_A_PREQUANT | H3FP4_EPI_SWIGLU | H3FP4_EPI_AMAX;
+                      H3FP4_A_PREQUANT | H3FP4_EPI_SWIGLU | H3FP4_EPI_AMAX | H3FP4_FUSED_QUANT;
     if (flags & ~known) return H3FP4_ERR_INVALID;
     const bool prequant = (flags & H3FP4_A_PREQUANT) != 0;
     const bool mod = (flags & H3FP4_PROLOGUE_MOD) != 0;
@@ -197,7 +199,10 @@ h3fp4_status h3fp4_linear(const void* x, const void* a_sf, const float* a_gscale
     const bool given = (flags & H3FP4_GSCALE_GIVEN) != 0;
     const bool swiglu = (flags & H3FP4_EPI_SWIGLU) != 0;
     const bool want_amax = (flags & H3FP4_EPI_AMAX) != 0;
+    const bool fused = (flags & H3FP4_FUSED_QUANT) != 0;
     if (swiglu && N % 256 != 0) return H3FP4_ERR_SHAPE;
+    if (fused && (prequant || swiglu)) return H3FP4_ERR_INVALID;
+    if (fused && (K + 255) / 256 > kPackMaxKStages) return H3FP4_ERR_SHAPE;
     if (swiglu && gated) return H3FP4_ERR_INVALID;
     if (!x || !w_codes || !w_sf || !w_gscale || !out_bf16 || !ws) return H3FP4_ERR_INVALID;
     if (prequant && (mod || !a_sf || !a_gscale)) return H3FP4_ERR_INVALID;
@@ -238,7 +243,20 @@ h3fp4_status h3fp4_linear(const void* x, const void* a_sf, const float* a_gscale
         q.gscale = given ? const_cast<float*>(a_gscale) : reinterpret_cast<float*>(wsb + kWsActGscale);
         q.gscale_given = given;
         q.partials = reinterpret_cast<float*>(wsb + kWsPartials);
-        if ((st = from_cuda(launch_quantize(q, stream))) != H3FP4_OK) return st;
+        if (fused) {
+            // amax pass (unless given); the GEMM kernel packs and consumes the tiles
+            int nparts = 0;
+            if (!given && (st = from_cuda(launch_amax_partials(q, &nparts, stream))) != H3FP4_OK) return st;
+            g.pk_x = x;
+            g.pk_shift = q.shift;
+            g.pk_scale = q.scale;
+            g.pk_partials = q.partials;
+            g.pk_nparts = nparts;
+            g.pk_given = given;
+            g.pk_flags = reinterpret_cast<uint32_t*>(q.sf + round256(h3fp4_sf_bytes(M, K)));
+        } else if ((st = from_cuda(launch_quantize(q, stream))) != H3FP4_OK) {
+            return st;
+        }
         g.a_codes = q.codes;
         g.a_sf = q.sf;
         g.a_gscale = q.gscale;
@@ -397,6 +415,38 @@ h3fp4_status h3fp4_selftest_timeout(void* ws, uint64_t limit_ns, cudaStream_t st
     g.status = reinterpret_cast<unsigned int*>(wsb + kWsStatus);
     g.wait_limit_ns = limit_ns ? limit_ns : 1;
     return from_cuda(launch_gemm_stall_selftest(g, stream));
+}
+
+h3fp4_status h3fp4_selftest_pack_timeout(const void* x_bf16, const float* a_gscale, void* ws, uint64_t limit_ns,
+                                         cudaStream_t stream)
+{
+    if (!x_bf16 || !a_gscale || !ws) return H3FP4_ERR_INVALID;
+    if (!aligned16(x_bf16) || !aligned16(ws) || (reinterpret_cast<uintptr_t>(a_gscale) & 3u)) return H3FP4_ERR_ALIGN;
+    h3fp4_status st = check_device();
+    if (st != H3FP4_OK) return st;
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+    const int64_t M = 128, N = 256, K = 256;
+    GemmJob g{};
+    // The packer writes the workspace's codes, scales and flags; the GEMM
+    // issues no copy (it never sees a published tile) and stores no output.
+    g.a_codes = wsb + kWsActCodes;
+    g.a_sf = wsb + kWsActCodes + round256(h3fp4_codes_bytes(M, K));
+    g.a_gscale = a_gscale;
+    g.w_codes = g.a_codes;
+    g.w_sf = g.a_sf;
+    g.w_gscale = a_gscale;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.out = wsb + kWsActCodes;
+    g.seg.nseg = 1;
+    g.seg.off[1] = M;
+    g.status = reinterpret_cast<unsigned int*>(wsb + kWsStatus);
+    g.wait_limit_ns = limit_ns ? limit_ns : 1;
+    g.pk_x = x_bf16;
+    g.pk_given = true;
+    g.pk_flags = reinterpret_cast<uint32_t*>(const_cast<uint8_t*>(g.a_sf) + round256(h3fp4_sf_bytes(M, K)));
+    return from_cuda(launch_gemm_pack_stall_selftest(g, stream));
 }
 
 h3fp4_status h3fp4_measure_fp4_peak(int iters, float* tflops, void* ws)

@@ -60,9 +60,11 @@
 // Each kernel launch may start while the previous kernel of the stream drains
 // (programmatic dependent launch); it reads no input before griddepcontrol.wait.
 // Registers per thread (setmaxnreg): warpgroup 0: 40, scale warps: 96,
-// epilogue: 184.  Per 128-thread warpgroup that is 40 + 96 + 2 x 184 = 504
+// epilogue: 184 (with the in-kernel packer 104 / 72 / 168).  Per 128-thread
+// warpgroup that is 40 + 96 + 2 x 184 = 504 (104 + 72 + 2 x 168 = 512)
 // registers per thread-slot, within the 4 x 128 the CTA is launched with.
 //
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
@@ -73,6 +75,7 @@
 #include "h3fp4_internal.h"
 #include "ptx_sm103.cuh"
 #include "nvfp4_encode.cuh"
+#include "act_prologue.cuh"
 
 namespace h3fp4 {
 namespace {
@@ -84,8 +87,17 @@ constexpr int kThreads = 512;
 constexpr int kScaleWarp0 = 4;   // warps 4..7: scale warps, lane quarter = warp & 3
 constexpr int kEpiWarp0 = 8;     // warps 8..15: epilogue
 constexpr int kEpiWarps = 8;
-constexpr uint32_t kRegsCtl = 40, kRegsScale = 96, kRegsEpi = 184;
-static_assert(128 * (kRegsCtl + kRegsScale + 2 * kRegsEpi) <= 65536, "setmaxnreg shares exceed the launch budget");
+// Registers per thread of each warpgroup (setmaxnreg): control (producer, MMA
+// issuer; with the in-kernel packer also the two packer warps), scale warps,
+// epilogue.  Each split sums to at most the 4 x 128 registers per thread-slot
+// the CTA is launched with.
+template <bool kPack>
+struct Regs {
+    static constexpr uint32_t kCtl = kPack ? 104 : 40;
+    static constexpr uint32_t kScale = kPack ? 72 : 96;
+    static constexpr uint32_t kEpi = kPack ? 168 : 184;
+    static_assert(128 * (kCtl + kScale + 2 * kEpi) <= 65536, "setmaxnreg shares exceed the launch budget");
+};
 constexpr uint32_t kABytes = BM * BK / 2;             // 16384
 constexpr uint32_t kBBytes = (BN / 2) * BK / 2;       // 16384: this CTA's half of W
 constexpr uint32_t kSFABytes = BM * (BK / 16);        // 2048: four 512-byte tiles
@@ -94,6 +106,9 @@ constexpr uint32_t kStageBytes = kABytes + kBBytes + kSFABytes + kSFBBytes;  // 
 constexpr uint32_t kPairTxBytes = 2 * (kABytes + kBBytes);  // both CTAs' code tiles complete on the leader
 constexpr uint32_t kSfBox = 2048;                     // scale-tile TMA box: 8 rows x 256 bytes
 constexpr uint32_t kChunkBytes = 32 * 32 * 2;         // 32 rows x 32 bf16
+constexpr uint32_t kXTileBytes = 32 * BK * 2;         // packer: 32 rows x 256 bf16 of X per TMA box
+constexpr uint32_t kPackThreads = 64;                 // packer: warps 2 and 3
+constexpr uint32_t kPackBar = 2;                      // packer: named barrier id
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmem = 256;
 constexpr uint32_t kSfTmemPerStage = 48;
@@ -105,19 +120,28 @@ static_assert(kStageBytes % 1024 == 0, "stages must keep the 1024-byte swizzle a
 // read the chunks.  The wide plan (gated residual epilogue over a short K
 // loop, where that epilogue is longer than a tile's mainloop) gives up one
 // stage for four chunks per warp: the whole tile's residual is loaded ahead
-// of the accumulator, and the epilogue runs in one pass.
+// of the accumulator, and the epilogue runs in one pass.  The pack plan (the
+// GEMM quantises its own activation) gives up one stage for two 16 KB X tiles
+// of the packer.
 // K stages per tile below which a gated residual epilogue takes the wide plan.
 constexpr int kWideMaxKStages = 24;
+static_assert(kXTileBytes % 1024 == 0, "X tiles keep the 1024-byte alignment");
 
-template <bool kWide>
+template <bool kWide, bool kPack>
 struct Plan {
-    static constexpr int kStages = kWide ? 4 : 5;
+    static_assert(!(kWide && kPack), "one plan at a time");
+    static constexpr int kStages = (kWide || kPack) ? 4 : 5;
     static constexpr int kChunks = kWide ? 4 : 2;               // staging chunks per epilogue warp
     static constexpr uint32_t kEpiWarpBytes = kChunks * kChunkBytes;
     static constexpr uint32_t kEpiOff = kStages * kStageBytes;
-    static constexpr uint32_t kBarOff = kEpiOff + kEpiWarps * kEpiWarpBytes;
-    static constexpr uint32_t kBarBytes = 8 * (3 * kStages + 3 + kEpiWarps) + 8;  // barriers, TMEM address, abort flag
-    static constexpr uint32_t kRcpOff = kBarOff + 512;          // kNvfp4: 128 fp32 block reciprocals of h
+    static constexpr uint32_t kXOff = kEpiOff + kEpiWarps * kEpiWarpBytes;  // kPack: two X tiles
+    static constexpr uint32_t kBarOff = kXOff + (kPack ? 2 * kXTileBytes : 0);
+    // barriers (full, empty, sf_full per stage; acc_full, acc_empty, done, one
+    // per epilogue warp; x_full x 2, sg_ready), TMEM address, abort flag,
+    // global scale of the packed activation, packer reduction slots
+    static constexpr uint32_t kBarBytes = 8 * (3 * kStages + 3 + kEpiWarps + 3) + 8 + 16;
+    static constexpr uint32_t kRcpOff = kBarOff + 512;          // kNvfp4: 128 fp32 block reciprocals of h;
+                                                                // kPack: of the packed activation
     static constexpr uint32_t kSmemBytes = kRcpOff + 512;
     static_assert(kBarBytes <= 512, "barrier block");
     static_assert(kSfTmem + kStages * kSfTmemPerStage <= kTmemCols, "TMEM budget");
@@ -141,13 +165,25 @@ struct GemmParams {
     Segments seg;
     unsigned int* status;
     unsigned long long wait_ns;
-    int stall;  // self-test: the producer issues nothing, so every consumer wait must time out
+    int stall;  // self-test: 1 = the producer issues nothing, so every consumer wait must time out;
+                //            2 = (kPack) the packer publishes no tile, so the producer's flag waits time out
     float* amax_out;  // kAmax: atomic max of |out| (bf16 values, as fp32 bits) over the call
     // kNvfp4: h written as NVFP4 under the caller's global scale of h
     uint8_t* h_codes;      // [M][N/4] bytes
     uint8_t* h_sf;         // block scales of h, 128x4-tiled, sf_bytes(M, N/2)
     const float* h_gscale; // device fp32
     int h_kb4;             // N/2/64 scale groups per row of h
+    // kPack: the activation quantised in-kernel (X bf16 [M][K] through tmX)
+    const float* pk_shift;    // [nseg][K] or null: the modulation prologue
+    const float* pk_scale;
+    uint8_t* pk_codes;        // out: [M][K/2] (what tmA reads)
+    uint8_t* pk_sf;           // out: block scales, 128x4-tiled (what tmSFA reads)
+    float* pk_gscale;         // in if pk_given, else out (written by CTA 0)
+    const float* pk_partials; // amax partials of the preceding amax pass
+    int pk_nparts;
+    int pk_given;
+    uint32_t* pk_flags;       // [m_tiles][k_stages] ready flags
+    uint32_t pk_epoch;        // the value a ready flag holds in this launch
 };
 
 __device__ __forceinline__ int segment_of_row(const Segments& s, int r)
@@ -168,6 +204,24 @@ __device__ __forceinline__ uint32_t swz64(uint32_t r, uint32_t j)
 
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
+// kPack: waits (bounded by limit_ns, or until the pair aborts) until *flag holds
+// v; acquire, so the tile the flag publishes is visible afterwards.
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t v, uint64_t limit_ns, unsigned int* err,
+                                          volatile int& abort)
+{
+    if (ld_acquire_gpu_u32(flag) == v) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(128);
+        if (ld_acquire_gpu_u32(flag) == v) return true;
+        if (abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            atomicOr(err, kStatusTimeoutPackFlag);
+            return false;
+        }
+    }
+}
+
 // silu(g) = g * sigmoid(g) in fp32.  With t = 2^(-|g| log2 e) in (0, 1],
 // sigmoid(g) = 1 / (1 + t) for g >= 0 and t / (1 + t) for g < 0, so no step
 // overflows for any g (e^-g itself overflows fp32 below g = -88.7).  Over every
@@ -184,17 +238,21 @@ __device__ __forceinline__ float silu_f32(float g)
 // kNvfp4 (with kSwiglu): h is not stored in bf16 but quantised to NVFP4 under the
 // given global scale of h, with the quantiser's arithmetic (nvfp4_encode.cuh).
 // Compile-time, so that the plain epilogue carries none of them.  kWide: the
-// wide plan (Plan above; gated residual epilogue only).
-template <bool kSwiglu, bool kAmax, bool kNvfp4, bool kWide>
+// wide plan (Plan above; gated residual epilogue only).  kPack: the kernel
+// quantises its activation itself (packer warps, below) instead of reading
+// codes a separate quantiser wrote.
+template <bool kSwiglu, bool kAmax, bool kNvfp4, bool kWide, bool kPack>
 __global__ void __launch_bounds__(kThreads, 1)
     nvfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmSFA, const __grid_constant__ CUtensorMap tmSFB,
                       const __grid_constant__ CUtensorMap tmOut, const __grid_constant__ CUtensorMap tmR,
-                      const GemmParams p)
+                      const __grid_constant__ CUtensorMap tmX, const GemmParams p)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     static_assert(!kWide || !kSwiglu, "the wide plan is for the gated residual epilogue");
-    using P = Plan<kWide>;
+    static_assert(!kPack || (!kSwiglu && !kNvfp4), "the in-kernel packer serves the plain and gated epilogues");
+    using P = Plan<kWide, kPack>;
+    using R = Regs<kPack>;
     constexpr int kStages = P::kStages;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -217,8 +275,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* acc_empty = acc_full + 1;                              // leader's: both epilogues drained
     uint64_t* rbar = acc_empty + 1;                                  // one per epilogue warp
     uint64_t* done_bar = rbar + kEpiWarps;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
+    uint64_t* x_full = done_bar + 1;                                 // kPack: the packer's two X tiles landed
+    uint64_t* sg_ready = x_full + 2;                                 // kPack: s_gscale holds the activation scale
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sg_ready + 1);
     volatile int& s_abort = *reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* s_gscale = reinterpret_cast<float*>(tmem_slot + 2);
+    float* s_red = s_gscale + 1;                                     // kPack: the packer warps' partial maxima
 
     if (threadIdx.x == 0) {
         s_abort = 0;
@@ -231,6 +293,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(acc_empty, 2 * kEpiWarps);
         for (int e = 0; e < kEpiWarps; ++e) mbar_init(&rbar[e], 1);
         mbar_init(done_bar, 1);
+        if (kPack) {
+            mbar_init(&x_full[0], 1);
+            mbar_init(&x_full[1], 1);
+            mbar_init(sg_ready, 1);
+        }
         fence_mbarrier_init();
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
@@ -238,6 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&tmSFB);
         prefetch_tensormap(&tmOut);
         if (p.has_resid) prefetch_tensormap(&tmR);
+        if (kPack) prefetch_tensormap(&tmX);
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, kTmemCols);
@@ -260,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     if (warp < kScaleWarp0) {
-        setmaxnreg_dec<kRegsCtl>();
+        setmaxnreg_dec<R::kCtl>();
         // The producer and the MMA issuer run as whole warps: every lane takes
         // the barrier waits (decided warp-wide), one elected lane issues the
         // copies / MMAs.  A single-lane loop around bounded waits measured far
@@ -271,16 +339,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t fills[kStages] = {};
-            for (int tile = blockIdx.x >> 1; tile < num_tiles && !p.stall; tile += gridDim.x >> 1) {
+            for (int tile = blockIdx.x >> 1; tile < num_tiles && p.stall != 1; tile += gridDim.x >> 1) {
                 if (__any_sync(0xffffffffu, s_abort != 0)) break;  // warp-uniform exit
                 const int mp = tile / p.n_tiles, nt = tile - mp * p.n_tiles;
                 const int mt = 2 * mp + (int)rank;  // this CTA's 128-row tile of A
                 bool ok = true;
+                // kPack: bit kb set once the packer published unit (mt, kb) (k_stages <= 64).
+                uint64_t rdy = ~0ull;
+                const uint32_t* flags = kPack ? p.pk_flags + (size_t)mt * (size_t)p.k_stages : nullptr;
+                auto poll = [&]() {
+                    uint64_t m = 0;
+                    for (int base = 0; base < p.k_stages; base += 32) {
+                        const int k = base + lane;
+                        const bool r = k < p.k_stages && ld_acquire_gpu_u32(flags + k) == p.pk_epoch;
+                        m |= (uint64_t)__ballot_sync(0xffffffffu, r) << base;
+                    }
+                    return m;
+                };
+                if (kPack && mt < p.m_tiles) rdy = poll();
                 for (int kb = 0; kb < p.k_stages; ++kb) {
                     ok = mbar_wait(&empty[stage], phase ^ 1u, p.wait_ns, p.status, kStatusTimeoutProducer);
                     if (!__all_sync(0xffffffffu, ok)) {
                         ok = false;
                         break;
+                    }
+                    if constexpr (kPack) {
+                        if (!((rdy >> kb) & 1ull)) {
+                            int r = 1;
+                            if (lane == 0) r = wait_flag(flags + kb, p.pk_epoch, p.wait_ns, p.status, s_abort) ? 1 : 0;
+                            if (!__shfl_sync(0xffffffffu, r, 0)) {
+                                ok = false;
+                                break;
+                            }
+                            rdy = poll() | (1ull << kb);
+                        }
+                        fence_proxy_async_global();  // the published codes and scales, before the TMA reads them
                     }
                     if (elect_one()) {
                         uint8_t* st = smem + stage * kStageBytes;
@@ -376,6 +469,170 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             (void)mbar_wait(done_bar, 0u, p.wait_ns, p.status, kStatusTimeoutMma);
             __syncwarp();
+        } else if (kPack && warp >= 2) {
+            // ------------------------------------------------------------ packer (both CTAs, kPack)
+            // Quantises the activation once, in units of one 128-row m-tile x one
+            // 256-column k-stage, with the quantiser's arithmetic (act_prologue.cuh,
+            // nvfp4_encode.cuh): same codes, block scales and global scale.  Each
+            // unit is published by a release store of its ready flag, which the
+            // producers of every CTA consuming that m-tile acquire before their
+            // TMA loads.  Units go to CTAs round-robin in the order the persistent
+            // schedule first needs them.  X comes in 32-row TMA tiles, two in flight.
+            const int pt = (int)threadIdx.x - 64;  // 0..63
+            float* a_rcp = reinterpret_cast<float*>(smem + P::kRcpOff);
+            float s_g;
+            if (p.pk_given) {
+                s_g = *p.pk_gscale;
+            } else {
+                // one full-activation amax over the amax pass's partials
+                float m = 0.0f;
+                for (int i = pt; i < p.pk_nparts; i += (int)kPackThreads) m = fmaxf(m, p.pk_partials[i]);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                if (lane == 0) s_red[warp - 2] = m;
+                named_bar_sync(kPackBar, kPackThreads);
+                const float amax = fmaxf(s_red[0], s_red[1]);
+                s_g = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 2688.0f);
+                if (blockIdx.x == 0 && pt == 0) *p.pk_gscale = s_g;
+            }
+            for (int c = pt; c < 128; c += (int)kPackThreads) a_rcp[c] = block_rcp((uint32_t)c, s_g);
+            named_bar_sync(kPackBar, kPackThreads);
+            if (pt == 0) {
+                *s_gscale = s_g;
+                mbar_arrive(sg_ready);  // the epilogue's alpha
+            }
+
+            const int ks = p.k_stages, mtiles = p.m_tiles;
+            const long long nunits = (long long)mtiles * ks;
+            const long long pairs = gridDim.x >> 1;
+            const long long K = p.K;
+            const bool mod = p.pk_shift != nullptr;
+            // First m-tile of group g: pair mp first appears in tile mp * n_tiles,
+            // i.e. in round mp * n_tiles / pairs of the persistent schedule.
+            auto group_first = [&](long long g) -> long long {
+                const long long mp = (g * pairs + p.n_tiles - 1) / p.n_tiles;
+                return min(2 * mp, (long long)mtiles);
+            };
+            long long grp = 0;
+            auto coords = [&](long long o, int& mt, int& kb) {
+                while (o >= group_first(grp + 1) * ks) ++grp;
+                const long long f = group_first(grp);
+                const long long nm = group_first(grp + 1) - f;
+                const long long rel = o - f * ks;
+                kb = (int)(rel / nm);
+                mt = (int)(f + rel % nm);
+            };
+            const long long my_units =
+                (long long)blockIdx.x < nunits ? (nunits - 1 - (long long)blockIdx.x) / gridDim.x + 1 : 0;
+            const long long T = 4 * my_units;  // jobs: 32-row X tiles
+            const int bc = pt & 15;            // this thread's 16-column block of a unit
+            const int rq = pt >> 4;            // its first row in an X tile (then every fourth)
+            ModCols mc;
+            init_mod(mc);
+            long long mc_cb = -1;
+            int cur_mt = 0, cur_kb = 0, nxt_mt = 0, nxt_kb = 0;
+            auto issue = [&](long long t, int mt, int kb) {
+                const int b = (int)(t & 1);
+                mbar_arrive_expect_tx(&x_full[b], kXTileBytes);
+                tma_load_2d(smem + P::kXOff + b * kXTileBytes, &tmX, &x_full[b], kb * BK,
+                            mt * BM + 32 * (int)(t & 3));
+            };
+            long long issued = 0, landed = 0;
+            if (T > 0) {
+                coords((long long)blockIdx.x, cur_mt, cur_kb);
+                if (pt == 0) issue(0, cur_mt, cur_kb);
+                issued = 1;
+            }
+            bool ok = true;
+            for (long long t = 0; t < T; ++t) {
+                // the next tile into the other buffer (its readers passed the barrier
+                // that ended the previous job)
+                if (t + 1 < T) {
+                    if (((t + 1) & 3) == 0)
+                        coords((long long)blockIdx.x + ((t + 1) >> 2) * gridDim.x, nxt_mt, nxt_kb);
+                    else {
+                        nxt_mt = cur_mt;
+                        nxt_kb = cur_kb;
+                    }
+                    if (pt == 0) issue(t + 1, nxt_mt, nxt_kb);
+                    ++issued;
+                }
+                const int b = (int)(t & 1);
+                bool got = mbar_wait(&x_full[b], (uint32_t)(t >> 1) & 1u, p.wait_ns, p.status, kStatusTimeoutPacker);
+                // one decision for all 64 packer threads (they share named barriers)
+                if (!named_bar_and(kPackBar, kPackThreads, got && s_abort == 0)) {
+                    ok = false;
+                    landed = got ? t + 1 : t;
+                    break;
+                }
+                landed = t + 1;
+                const uint8_t* xt = smem + P::kXOff + b * kXTileBytes;
+                const long long row0 = (long long)cur_mt * BM + 32 * (t & 3);
+                const long long cb = (long long)cur_kb * 16 + bc;  // 16-column block index in the row
+                const bool colv = cb < K / 16;
+                if (mod && colv && cb != mc_cb) {
+                    mc_cb = cb;
+                    mc.seg_end = -1;  // reload the constants of the new column block
+                }
+#pragma unroll 1
+                for (int j = 0; j < 8; ++j) {
+                    const int rl = rq + 4 * j;
+                    const long long row = row0 + rl;
+                    const bool real = row < p.M;
+                    const uint32_t xa = smem_u32(xt) + (uint32_t)rl * (BK * 2) + (uint32_t)bc * 32u;
+                    const uint4 v0 = ld_shared_v4(xa), v1 = ld_shared_v4(xa + 16u);
+                    V16 v;
+                    v.w[0] = v0.x; v.w[1] = v0.y; v.w[2] = v0.z; v.w[3] = v0.w;
+                    v.w[4] = v1.x; v.w[5] = v1.y; v.w[6] = v1.z; v.w[7] = v1.w;
+                    float f[16];
+                    unpack16(v, f);
+                    if (mod && real && colv) {
+                        if (row >= mc.seg_end || row < mc.seg_begin)
+                            load_mod(p.pk_scale, p.pk_shift, K, p.seg, segment_of(p.seg, row), cb, mc);
+                        modulate16<true>(f, mc);
+                    }
+                    float bmax = 0.0f;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(f[i]));
+                    const uint32_t S = real ? block_scale_code(bmax, s_g) : 0u;  // padding rows: zero scales
+                    const float rcp = a_rcp[S & 127u];
+                    const uint64_t rcp2 = f2(rcp, rcp);
+                    float q[16];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) unf2(mul2(f2(f[2 * i], f[2 * i + 1]), rcp2), q[2 * i], q[2 * i + 1]);
+                    const uint32_t w0 = e2m1x8(reinterpret_cast<const float(&)[8]>(q[0]));
+                    const uint32_t w1 = e2m1x8(reinterpret_cast<const float(&)[8]>(q[8]));
+                    if (real && colv)
+                        *reinterpret_cast<uint2*>(p.pk_codes + row * (K / 2) + cb * 8) = make_uint2(w0, w1);
+                    // the four block scales of a 64-column group into its first lane
+                    const uint32_t s1 = __shfl_down_sync(0xffffffffu, S, 1);
+                    const uint32_t s2 = __shfl_down_sync(0xffffffffu, S, 2);
+                    const uint32_t s3 = __shfl_down_sync(0xffffffffu, S, 3);
+                    if (colv && (bc & 3) == 0) {
+                        const long long g = cb >> 2;
+                        const uint32_t r7 = (uint32_t)row & 127u;
+                        const long long off = (((row >> 7) * p.kb4 + g) << 9) + ((r7 & 31u) << 4) + ((r7 >> 5) << 2);
+                        *reinterpret_cast<uint32_t*>(p.pk_sf + off) = S | (s1 << 8) | (s2 << 16) | (s3 << 24);
+                    }
+                }
+                const bool last = (t & 3) == 3;
+                fence_proxy_async_smem();  // this job's reads of the X tile, before its refill
+                if (last) {
+                    fence_proxy_async_global();  // the unit's codes and scales, for TMA readers
+                    __threadfence();
+                }
+                named_bar_sync(kPackBar, kPackThreads);
+                if (last && pt == 0 && p.stall != 2)
+                    st_release_gpu_u32(p.pk_flags + (size_t)cur_mt * (size_t)ks + cur_kb, p.pk_epoch);
+                cur_mt = nxt_mt;
+                cur_kb = nxt_kb;
+            }
+            if (!ok) {
+                if (pt == 0) set_abort();
+                // tiles still in flight must land before the CTA may exit
+                for (long long t = landed; t < issued; ++t)
+                    (void)mbar_wait(&x_full[t & 1], (uint32_t)(t >> 1) & 1u, p.wait_ns, p.status, kStatusTimeoutPacker);
+            }
         }
     } else if (warp < kEpiWarp0) {
         // ---------------------------------------------------------------- scale warps (both CTAs)
@@ -385,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // -- the TMEM image the MMA reads (each quarter a full copy).
         // The TMEM slot of a stage is rewritten only after the stage was refilled,
         // i.e. after the MMAs that read the previous contents committed.
-        setmaxnreg_dec<kRegsScale>();
+        setmaxnreg_dec<R::kScale>();
         const uint32_t q = (uint32_t)(warp & 3);
         const uint32_t ready_leader = mapa_shared(smem_u32(full), 0);
         int stage = 0;
@@ -440,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------------------------------------------------------- epilogue (both CTAs)
-        setmaxnreg_inc<kRegsEpi>();
+        setmaxnreg_inc<R::kEpi>();
         const int e = warp - kEpiWarp0;    // 0..7
         float* rcp_tab = reinterpret_cast<float*>(smem + P::kRcpOff);
         if constexpr (kNvfp4) {
@@ -454,7 +711,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;            // TMEM lane quarter this warp may access
         const int h = e >> 2;              // column half of the 256-wide tile
         uint8_t* stg = smem + P::kEpiOff + e * P::kEpiWarpBytes;
-        const float alpha = __fmul_rn(__ldg(p.a_gscale), __ldg(p.w_gscale));
+        float a_s;
+        if constexpr (kPack) {
+            // the packer's global scale of the activation (it may be computing it in this launch)
+            a_s = mbar_wait(sg_ready, 0u, p.wait_ns, p.status, kStatusTimeoutEpilogue) ? *s_gscale : 0.0f;
+        } else {
+            a_s = __ldg(p.a_gscale);
+        }
+        const float alpha = __fmul_rn(a_s, __ldg(p.w_gscale));
         const uint64_t alpha2 = f2(alpha, alpha);
         uint32_t acc_phase = 0, r_phase = 0;
         bool r_pending = false;
@@ -754,6 +1018,8 @@ cudaError_t launch_gemm(const GemmJob& job, cudaStream_t s) { return launch_gemm
 
 cudaError_t launch_gemm_stall_selftest(const GemmJob& job, cudaStream_t s) { return launch_gemm_impl(job, 1, s); }
 
+cudaError_t launch_gemm_pack_stall_selftest(const GemmJob& job, cudaStream_t s) { return launch_gemm_impl(job, 2, s); }
+
 // Largest number of CTA pairs that can be resident at once on the current
 // device (GPCs with an odd number of free SMs leave one SM idle), cached per device.
 static int max_pairs_current_device()
@@ -772,13 +1038,14 @@ static int max_pairs_current_device()
         attr[0].val.clusterDim.z = 1;
         cfg.gridDim = dim3(2 * (unsigned)sm_count_current_device());
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = Plan<false>::kSmemBytes;  // one CTA per SM with either plan
+        cfg.dynamicSmemBytes = Plan<false, false>::kSmemBytes;  // one CTA per SM with every plan
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int n = 0;
-        const void* probe = reinterpret_cast<const void*>(nvfp4_gemm_kernel<false, false, false, false>);
-        if (ensure_dynamic_smem(probe, (int)Plan<false>::kSmemBytes) != cudaSuccess ||
-            cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel<false, false, false, false>, &cfg) != cudaSuccess ||
+        const void* probe = reinterpret_cast<const void*>(nvfp4_gemm_kernel<false, false, false, false, false>);
+        if (ensure_dynamic_smem(probe, (int)Plan<false, false>::kSmemBytes) != cudaSuccess ||
+            cudaOccupancyMaxActiveClusters(&n, nvfp4_gemm_kernel<false, false, false, false, false>, &cfg) !=
+                cudaSuccess ||
             n <= 0)
             n = sm_count_current_device() / 2;
         cache[dev] = n;
@@ -788,7 +1055,10 @@ static int max_pairs_current_device()
 
 static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t s)
 {
-    CUtensorMap tmA, tmB, tmSFA, tmSFB, tmOut, tmR;
+    CUtensorMap tmA, tmB, tmSFA, tmSFB, tmOut, tmR, tmX;
+    const bool pack = job.pk_x != nullptr;
+    if (pack && (job.swiglu || job.h_codes != nullptr || (job.K + BK - 1) / BK > kPackMaxKStages))
+        return cudaErrorInvalidValue;
     const uint64_t kbytes = (uint64_t)job.K / 2;
     const int64_t m_tiles = (job.M + BM - 1) / BM;
     const int64_t n_sf_tiles = (job.N + 127) / 128;
@@ -811,7 +1081,11 @@ static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t 
                      job.h_codes ? (uint64_t)job.N / 4 : out_cols * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map_2d(&tmR, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                      job.resid ? job.resid : (job.out ? job.out : (const void*)job.h_codes), (uint64_t)job.N,
-                     (uint64_t)job.M, (uint64_t)job.N * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+                     (uint64_t)job.M, (uint64_t)job.N * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        // the packer's X tiles: 32 rows x 256 columns (without the packer a valid stand-in)
+        !make_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, pack ? job.pk_x : (const void*)job.a_codes,
+                     pack ? (uint64_t)job.K : kbytes / 2, (uint64_t)job.M, pack ? (uint64_t)job.K * 2 : kbytes,
+                     BK, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
 
     GemmParams p{};
@@ -837,17 +1111,40 @@ static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t 
     p.h_sf = job.h_sf;
     p.h_gscale = job.h_gscale;
     p.h_kb4 = (int)(job.N / 128);
+    if (pack) {
+        // Call numbers: a fixed odd stride walks all 2^32 values before it
+        // repeats, so flags left by earlier calls never hold this call's
+        // number; 0 (a zeroed workspace) is skipped.
+        static std::atomic<uint32_t> calls{0};
+        uint32_t e = 0;
+        while (e == 0) e = (calls.fetch_add(1) + 1) * 0x9E3779B1u;
+        p.pk_shift = job.pk_shift;
+        p.pk_scale = job.pk_scale;
+        p.pk_codes = const_cast<uint8_t*>(job.a_codes);
+        p.pk_sf = const_cast<uint8_t*>(job.a_sf);
+        p.pk_gscale = const_cast<float*>(job.a_gscale);
+        p.pk_partials = job.pk_partials;
+        p.pk_nparts = job.pk_nparts;
+        p.pk_given = job.pk_given ? 1 : 0;
+        p.pk_flags = job.pk_flags;
+        p.pk_epoch = e;
+    }
 
-    // The wide plan where a tile's gated epilogue outlasts its mainloop (short K).
-    const bool wide = p.has_resid && !job.swiglu && job.h_codes == nullptr && p.k_stages < kWideMaxKStages;
-    auto kernel = job.h_codes != nullptr ? nvfp4_gemm_kernel<true, false, true, false>
-                  : job.swiglu ? (job.amax_out ? nvfp4_gemm_kernel<true, true, false, false>
-                                               : nvfp4_gemm_kernel<true, false, false, false>)
-                  : wide ? (job.amax_out ? nvfp4_gemm_kernel<false, true, false, true>
-                                         : nvfp4_gemm_kernel<false, false, false, true>)
-                         : (job.amax_out ? nvfp4_gemm_kernel<false, true, false, false>
-                                         : nvfp4_gemm_kernel<false, false, false, false>);
-    const uint32_t smem_bytes = wide ? Plan<true>::kSmemBytes : Plan<false>::kSmemBytes;
+    // The wide plan where a tile's gated epilogue outlasts its mainloop (short
+    // K); the pack plan when the kernel quantises its own activation.
+    const bool wide = !pack && p.has_resid && !job.swiglu && job.h_codes == nullptr && p.k_stages < kWideMaxKStages;
+    auto kernel = pack ? (job.amax_out ? nvfp4_gemm_kernel<false, true, false, false, true>
+                                       : nvfp4_gemm_kernel<false, false, false, false, true>)
+                  : job.h_codes != nullptr ? nvfp4_gemm_kernel<true, false, true, false, false>
+                  : job.swiglu ? (job.amax_out ? nvfp4_gemm_kernel<true, true, false, false, false>
+                                               : nvfp4_gemm_kernel<true, false, false, false, false>)
+                  : wide ? (job.amax_out ? nvfp4_gemm_kernel<false, true, false, true, false>
+                                         : nvfp4_gemm_kernel<false, false, false, true, false>)
+                         : (job.amax_out ? nvfp4_gemm_kernel<false, true, false, false, false>
+                                         : nvfp4_gemm_kernel<false, false, false, false, false>);
+    const uint32_t smem_bytes = pack   ? Plan<false, true>::kSmemBytes
+                                : wide ? Plan<true, false>::kSmemBytes
+                                       : Plan<false, false>::kSmemBytes;
     const cudaError_t attr_err = ensure_dynamic_smem(reinterpret_cast<const void*>(kernel), (int)smem_bytes);
     if (attr_err != cudaSuccess) return attr_err;
 
@@ -869,7 +1166,7 @@ static cudaError_t launch_gemm_impl(const GemmJob& job, int stall, cudaStream_t 
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmSFA, tmSFB, tmOut, tmR, p);
+    return cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmSFA, tmSFB, tmOut, tmR, tmX, p);
 }
 
 }  // namespace h3fp4

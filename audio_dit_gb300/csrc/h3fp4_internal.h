@@ -20,6 +20,8 @@ constexpr unsigned int kStatusTimeoutProducer = 1u;
 constexpr unsigned int kStatusTimeoutMma = 2u;
 constexpr unsigned int kStatusTimeoutEpilogue = 4u;
 constexpr unsigned int kStatusBadSmemAlign = 8u;
+constexpr unsigned int kStatusTimeoutPackFlag = 16u;  // GEMM producer: an activation tile never published
+constexpr unsigned int kStatusTimeoutPacker = 32u;    // in-kernel packer: an X tile never landed
 
 struct Segments {
     int nseg;
@@ -64,13 +66,38 @@ struct GemmJob {
     uint8_t* h_codes;
     uint8_t* h_sf;
     const float* h_gscale;
+    // In-kernel quantisation of the activation (plain or gated epilogue): the
+    // kernel's packer warps write a_codes / a_sf from X (and, unless
+    // pk_given, the global scale into a_gscale from the amax pass's partials)
+    // while its GEMM consumes them.  Null pk_x: a_codes / a_sf are inputs.
+    const void* pk_x;         // bf16 [M][K]
+    const float* pk_shift;    // [nseg][K] or null
+    const float* pk_scale;
+    const float* pk_partials;
+    int pk_nparts;
+    bool pk_given;
+    uint32_t* pk_flags;       // pack_flag_words(M, K) words, owned by the call
 };
+
+// Ready-flag words the in-kernel quantisation needs: one per (128-row tile,
+// 256-column stage) of the activation.
+inline size_t pack_flag_words(int64_t M, int64_t K) { return (size_t)((M + 127) / 128) * (size_t)((K + 255) / 256); }
+
+// K stages per tile the in-kernel quantisation supports (K <= 16384).
+constexpr int kPackMaxKStages = 64;
+
+// Launches only the amax pass; *nparts receives the number of partials it writes.
+cudaError_t launch_amax_partials(const QuantJob& job, int* nparts, cudaStream_t s);
 
 cudaError_t launch_gemm(const GemmJob& job, cudaStream_t s);
 
 // The same GEMM kernel with its producer disabled: every consumer wait runs out,
 // the kernel records a timeout in the status word and returns (self-test).
 cudaError_t launch_gemm_stall_selftest(const GemmJob& job, cudaStream_t s);
+
+// The in-kernel quantisation with its packer publishing no tile: every wait of
+// the producer for a tile runs out (self-test).
+cudaError_t launch_gemm_pack_stall_selftest(const GemmJob& job, cudaStream_t s);
 
 // Global amax of the (modulated) activation into amax_out (device fp32).
 cudaError_t launch_amax(const QuantJob& job, float* amax_out, cudaStream_t s);

@@ -24,6 +24,7 @@
 #include "h3fp4_internal.h"
 #include "ptx_sm103.cuh"
 #include "nvfp4_encode.cuh"
+#include "act_prologue.cuh"
 
 namespace h3fp4 {
 namespace {
@@ -54,15 +55,8 @@ struct QuantParams {
     int rows_per_cta;
 };
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
 // Sixteen bf16 values = 32 bytes: one 256-bit load when the row pointer is
 // 32-byte aligned, two 128-bit loads otherwise.
-struct V16 {
-    uint32_t w[8];
-};
-
 template <bool kWide>
 __device__ __forceinline__ V16 ld16(const uint16_t* p)
 {
@@ -79,76 +73,6 @@ __device__ __forceinline__ V16 ld16(const uint16_t* p)
         v.w[4] = b.x; v.w[5] = b.y; v.w[6] = b.z; v.w[7] = b.w;
     }
     return v;
-}
-
-__device__ __forceinline__ void unpack16(const V16& v, float (&f)[16])
-{
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        f[2 * i] = bf16_lo(v.w[i]);
-        f[2 * i + 1] = bf16_hi(v.w[i]);
-    }
-}
-
-__device__ __forceinline__ int segment_of(const Segments& s, long long r)
-{
-    int i = 0;
-#pragma unroll 1
-    while (i + 1 < s.nseg && r >= s.off[i + 1]) ++i;
-    return i;
-}
-
-// Per-thread modulation constants for the 16 columns it owns.
-struct ModCols {
-    uint64_t onep[8], sh[8];  // (1 + scale, shift) of columns 2j, 2j + 1
-    long long seg_begin, seg_end;  // rows [seg_begin, seg_end) use these constants
-};
-
-__device__ __forceinline__ void load_mod(const QuantParams& p, int seg, int cb, ModCols& mc)
-{
-    const float4* sc = reinterpret_cast<const float4*>(p.scale + (long long)seg * p.K + (long long)cb * 16);
-    const float4* sh = reinterpret_cast<const float4*>(p.shift + (long long)seg * p.K + (long long)cb * 16);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float4 a = __ldg(sc + i);
-        const float4 b = __ldg(sh + i);
-        mc.onep[2 * i] = f2(__fadd_rn(1.0f, a.x), __fadd_rn(1.0f, a.y));
-        mc.onep[2 * i + 1] = f2(__fadd_rn(1.0f, a.z), __fadd_rn(1.0f, a.w));
-        mc.sh[2 * i] = f2(b.x, b.y);
-        mc.sh[2 * i + 1] = f2(b.z, b.w);
-    }
-    mc.seg_begin = p.seg.off[seg];
-    mc.seg_end = p.seg.off[seg + 1];
-}
-
-__device__ __forceinline__ void init_mod(ModCols& mc)
-{
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        mc.onep[j] = f2(1.0f, 1.0f);
-        mc.sh[j] = f2(0.0f, 0.0f);
-    }
-    mc.seg_begin = 0;
-    mc.seg_end = -1;
-}
-
-// m = bf16(fma(x, 1 + scale, shift)) for 16 values: one fp32 fma each, then one
-// packed round-to-nearest-even conversion per pair (cvt.rn.bf16x2.f32 rounds
-// each half exactly like the scalar conversion, at half the conversion cost).
-template <bool kMod>
-__device__ __forceinline__ void modulate16(float (&f)[16], const ModCols& mc)
-{
-    if (kMod) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float a, b;
-            unf2(fma2(f2(f[2 * j], f[2 * j + 1]), mc.onep[j], mc.sh[j]), a, b);
-            const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-            const uint32_t u = *reinterpret_cast<const uint32_t*>(&h);
-            f[2 * j] = bf16_lo(u);
-            f[2 * j + 1] = bf16_hi(u);
-        }
-    }
 }
 
 __device__ __forceinline__ float block_reduce_max(float v, float* red)
@@ -191,7 +115,7 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(QuantParams p)
 #pragma unroll
         for (int u = 0; u < kRowUnroll; ++u) {
             if (!(valid && u < n)) continue;
-            if (kMod && r + u >= mc.seg_end) load_mod(p, segment_of(p.seg, r + u), cb, mc);
+            if (kMod && r + u >= mc.seg_end) load_mod(p.scale, p.shift, p.K, p.seg, segment_of(p.seg, r + u), cb, mc);
             float f[16];
             unpack16(v[u], f);
             if (kMod) {
@@ -271,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 10) pack_kernel(QuantParams p)
             float f[16];
             unpack16(v[u], f);
             if (kMod) {
-                if ((rr >= mc.seg_end || rr < mc.seg_begin) && valid) load_mod(p, segment_of(p.seg, rr), cb, mc);
+                if ((rr >= mc.seg_end || rr < mc.seg_begin) && valid) load_mod(p.scale, p.shift, p.K, p.seg, segment_of(p.seg, rr), cb, mc);
                 modulate16<kMod>(f, mc);
             }
             float bmax = 0.0f;
@@ -431,6 +355,15 @@ cudaError_t launch_quantize(const QuantJob& job, cudaStream_t s)
         if (e != cudaSuccess) return e;
     }
     return mod ? launch_pack_t<true>(pp, pgrid, wide, s) : launch_pack_t<false>(pp, pgrid, wide, s);
+}
+
+cudaError_t launch_amax_partials(const QuantJob& job, int* nparts, cudaStream_t s)
+{
+    dim3 grid;
+    const QuantParams p = make_params(job, amax_ctas_per_sm(), &grid);
+    *nparts = p.nparts;
+    return job.shift != nullptr ? launch_amax_t<true>(p, grid, wide_ok(job.x), s)
+                                : launch_amax_t<false>(p, grid, wide_ok(job.x), s);
 }
 
 cudaError_t launch_amax(const QuantJob& job, float* amax_out, cudaStream_t s)

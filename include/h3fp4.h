@@ -100,7 +100,8 @@ enum {
     H3FP4_GSCALE_GIVEN = 16,   /* activation global scale read from a_gscale (device fp32 > 0)     */
     H3FP4_A_PREQUANT = 32,     /* x is already NVFP4: codes + a_sf + a_gscale                     */
     H3FP4_EPI_SWIGLU = 64,     /* out[M][N/2] = bf16(silu(g) * u), see h3fp4_linear                */
-    H3FP4_EPI_AMAX = 128       /* also write max|out| to h3fp4_ws_out_amax(ws)                    */
+    H3FP4_EPI_AMAX = 128,      /* also write max|out| to h3fp4_ws_out_amax(ws)                    */
+    H3FP4_FUSED_QUANT = 256    /* quantise x inside the GEMM kernel, see h3fp4_linear              */
 };
 
 #define H3FP4_MAX_SEGMENTS 8
@@ -115,9 +116,12 @@ H3FP4_API size_t h3fp4_sf_bytes(int64_t rows, int64_t K);
 /* Workspace bytes h3fp4_linear needs for (M, N, K, flags); also enough for
  * h3fp4_quantize_act / h3fp4_quantize_weight of M (or N) rows.  Holds the
  * device status word, the amax partial maxima and, unless A_PREQUANT, the
- * activation's codes, block scales and global scale.  Zero the first 256
- * bytes (the status word) once before first use; concurrent calls must not
- * share one workspace. */
+ * activation's codes, block scales, global scale and (H3FP4_FUSED_QUANT)
+ * the ready flags of its tiles.  Zero the workspace (at least the status word,
+ * its first 256 bytes, and the flags) once before first use, and write it
+ * with nothing but this library afterwards: the flags hold call numbers that
+ * never repeat within a process.  Concurrent calls must not share one
+ * workspace. */
 H3FP4_API size_t h3fp4_workspace_bytes(int64_t M, int64_t N, int64_t K, int flags);
 
 /* Quantise a weight W [N, K] bf16 to NVFP4 (offline step; same algorithm as
@@ -184,7 +188,18 @@ H3FP4_API h3fp4_status h3fp4_quantize_act(const void* x_bf16, int64_t M, int64_t
  * h3fp4_ws_out_amax(ws).  A following h3fp4_gscale_from_amax and
  * H3FP4_GSCALE_GIVEN quantisation of `out` (no prologue) then produce the
  * same codes, block scales and global scale as the two-pass quantisation,
- * with one pass over `out` instead of two. */
+ * with one pass over `out` instead of two.
+ *
+ * Quantise-once producer (H3FP4_FUSED_QUANT; "H3 Runtime Current State",
+ * "Owned Performance Kernels": a producer that quantises each (M, K) tile
+ * once and shares it across the N consumers, with one full-activation
+ * scale): the GEMM kernel's packer warps quantise x tile by tile (128 rows x
+ * 256 columns) into the workspace while the same kernel's GEMM consumes the
+ * tiles, each behind a ready flag it waits for (bounded; a timeout is
+ * reported by h3fp4_check).  With the computed scale an amax pass runs
+ * first; with H3FP4_GSCALE_GIVEN the GEMM kernel is the only launch.  Codes,
+ * block scales, global scale and out are the bytes of the two-pass path.
+ * Not with H3FP4_A_PREQUANT or H3FP4_EPI_SWIGLU; K <= 16384. */
 H3FP4_API h3fp4_status h3fp4_linear(const void* x, const void* a_sf, const float* a_gscale,
                           int64_t M, int64_t N, int64_t K,
                           const void* w_codes, const void* w_sf, const float* w_gscale,
@@ -272,6 +287,15 @@ H3FP4_API h3fp4_status h3fp4_gscale_from_amax(const float* amax, float* gscale, 
  * its TMEM and returns.  h3fp4_check(ws) must afterwards report
  * H3FP4_ERR_TIMEOUT.  No data is read or written besides the status word. */
 H3FP4_API h3fp4_status h3fp4_selftest_timeout(void* ws, uint64_t limit_ns, cudaStream_t stream);
+
+/* The same for the quantise-once producer's ready flags: the fused GEMM
+ * (H3FP4_FUSED_QUANT, given scale *a_gscale) on a 128x256x256 problem whose
+ * packer quantises x (bf16 [128][256], device) into the workspace but
+ * publishes no tile, so the GEMM's waits for the tiles run out after
+ * limit_ns and the kernel returns.  ws: h3fp4_workspace_bytes(128, 256, 256,
+ * 0) bytes; h3fp4_check(ws) must afterwards report H3FP4_ERR_TIMEOUT. */
+H3FP4_API h3fp4_status h3fp4_selftest_pack_timeout(const void* x_bf16, const float* a_gscale, void* ws,
+                                                   uint64_t limit_ns, cudaStream_t stream);
 
 /* Measured tensor-core ceiling for the GEMM's instruction on the current
  * device: back-to-back tcgen05.mma.kind::mxf4nvf4.block_scale (M=128, N=256,
