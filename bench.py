@@ -188,6 +188,40 @@ class Problem:
         return b
 
 
+def time_fused_quant(torch, A, prob: Problem, steps: int, flush):
+    """The quantise-once producer inside the GEMM (h3fp4_linear with
+    H3FP4_FUSED_QUANT): per step, the amax pass and the GEMM kernel that packs
+    its own activation; and with a caller-given global scale, that kernel
+    alone.  CUDA events around the public call, L2 flushed between steps."""
+    s = torch.cuda.current_stream()
+    gs = torch.empty(1, dtype=torch.float32, device="cuda")
+    prob.quant(A)
+    gs.copy_(prob.aq[2])
+    kw = dict(shift=prob.shift, scale=prob.scale, gate=prob.gate, resid=prob.resid, bias=prob.bias,
+              seg_off=prob.seg_off, fused=True)
+    res = {}
+    for key, extra in (("tflops", {}), ("given_scale_tflops", {"a_gscale": gs, "gscale_given": True})):
+        call = lambda: A.h3fp4_linear(prob.x, *prob.wq, prob.out, prob.ws, **kw, **extra)
+        for _ in range(3):
+            flush()
+            call()
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for i in range(steps):
+            flush()
+            ev[i][0].record(s)
+            call()
+            ev[i][1].record(s)
+        torch.cuda.synchronize()
+        ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+        res[key] = round(prob.flops / (ms * 1e-3) / 1e12, 1)
+        res[key.replace("tflops", "ms")] = round(ms, 4)
+    A.h3fp4_check(prob.ws)
+    res["note"] = ("GEMM kernel quantising its own activation (packer warps, per-tile ready flags); "
+                   "in-run scale: amax pass + that kernel")
+    return res
+
+
 def time_mlp_chain(torch, A, steps: int, warmup: int, flush):
     """MLP FC1 -> SwiGLU -> FC2 through the public call, X [32768, 3072] with the
     fc1 recipe and modulation, W1 [24576, 3072] in [gate 128 | up 128] row groups,
@@ -601,13 +635,14 @@ def run_gpu(args):
     quant_ms = float(np.mean(q))
     quant_gbs = (qb["amax"] + qb["pack"]) / (quant_ms * 1e-3) / 1e9
 
-    given = None
+    given = fused_q = None
     if rank == 0:
         qg, gg, _ = time_device_steps(torch, A, prob, max(5, min(500, args.steps // 4)), 3, flush, given_scale=True)
         given = {"tflops": round(prob.flops / (np.mean(qg + gg) * 1e-3) / 1e12, 1),
                  "quant_ms": round(float(np.mean(qg)), 5),
                  "quant_gbs": round(qb["pack_given"] / (np.mean(qg) * 1e-3) / 1e9, 1),
                  "note": "global scale supplied by the caller: pack pass + GEMM"}
+        fused_q = time_fused_quant(torch, A, prob, max(5, min(200, args.steps // 4)), flush)
 
     extra = {}
     if rank == 0 and not args.no_extra:
@@ -627,6 +662,9 @@ def run_gpu(args):
                     "given_scale_tflops": round(pe.flops / (np.mean(qge + gge) * 1e-3) / 1e12, 1),
                     "given_scale_quant_gbs": round(qbe["pack_given"] / (np.mean(qge) * 1e-3) / 1e9, 1),
                 }
+                if name != "tiny":
+                    extra[name]["fused_quant"] = time_fused_quant(torch, A, pe, max(5, min(100, args.steps // 8)),
+                                                                  flush)
                 del pe
                 torch.cuda.empty_cache()
             except Exception as e:  # a failing extra config must not hide the headline
@@ -713,6 +751,8 @@ def run_gpu(args):
         }
         if given:
             line["given_scale"] = given
+        if fused_q is not None:
+            line["fused_quant"] = fused_q
         if extra:
             line["also"] = extra
         if cpu:
