@@ -36,10 +36,14 @@
 //   warp 0      TMA producer (both CTAs): per stage first this CTA's
 //               block-scale tiles (on its own "scales landed" barrier), then
 //               the A / W code tiles (128-byte swizzle), whose bytes complete
-//               on the LEADER's "full" barrier (5-stage ring).
+//               on the LEADER's "full" barrier (5-stage ring; 4 with the wide
+//               and pack plans).
 //   warp 1      TMEM owner (both) + MMA issuer (leader): per stage, one wait
 //               on the leader's "full", four paired MMAs, then a commit
 //               multicast to both CTAs' "empty" barrier.
+//   warps 2-3   (kPack only) packer (both): quantise 128 x 256 units of X
+//               into the codes / scales the producer loads, each published by
+//               a ready flag the producer acquires before its A loads.
 //   warps 4-7   scale warps (both), warp 4 + q serving lane quarter q: per
 //               stage, as soon as the CTA's scale tiles landed, twelve 16-byte
 //               shared loads per lane, tcgen05.st of 48 columns, then an
