@@ -38,6 +38,10 @@ def test_size_queries(lib):
     assert A.h3fp4_sf_bytes(129, 3072) == 256 * 3072 // 16
     ws = A.h3fp4_workspace_bytes(300, 1024, 512, 0)
     assert ws >= A.h3fp4_codes_bytes(300, 512) + A.h3fp4_sf_bytes(300, 512)
+    # codes, scales and one ready flag per (128-row, 256-column) tile on top of the pre-quantised size
+    flags = ((300 + 127) // 128) * ((512 + 255) // 256)
+    assert ws - A.h3fp4_workspace_bytes(300, 1024, 512, A.A_PREQUANT) >= (
+        A.h3fp4_codes_bytes(300, 512) + A.h3fp4_sf_bytes(300, 512) + 4 * flags)
     assert A.h3fp4_workspace_bytes(300, 1024, 512, A.A_PREQUANT) < ws
 
 
@@ -70,6 +74,14 @@ def test_host_validation_rejects_before_launch(lib):
                             None, None, dummy, 64, dummy, None) == 2
     assert lib.h3fp4_linear(dummy, None, None, 16, 256, 64, dummy, dummy, dummy, None, None, dummy, None, 1,
                             None, dummy, dummy, 64 | 4, dummy, None) == 1
+    # the quantise-once producer inside the GEMM: not with a pre-quantised
+    # activation or the SwiGLU epilogue, and K at most 64 stages of 256
+    assert lib.h3fp4_linear(dummy, dummy, dummy, 16, 16, 64, dummy, dummy, dummy, None, None, None, None, 1,
+                            None, None, vp(8192), 256 | 32, dummy, None) == 1
+    assert lib.h3fp4_linear(dummy, None, None, 16, 256, 64, dummy, dummy, dummy, None, None, None, None, 1,
+                            None, None, vp(8192), 256 | 64, dummy, None) == 1
+    assert lib.h3fp4_linear(dummy, None, None, 16, 16, 16384 + 64, dummy, dummy, dummy, None, None, None, None, 1,
+                            None, None, vp(8192), 256, dummy, None) == 2
     assert lib.h3fp4_status_string(5) == b"device wait timed out"
 
 
@@ -108,7 +120,7 @@ def test_swiglu_and_amax_flags_pass_host_validation(lib):
         pytest.skip("fake device pointers: host-validation check runs only without a CUDA device")
     vp = C.c_void_p
     dummy = vp(4096)
-    for flags in (64, 128, 64 | 128, 64 | 128 | 2 | 1):
+    for flags in (64, 128, 64 | 128, 64 | 128 | 2 | 1, 256, 256 | 128 | 2 | 1):
         shift = dummy if flags & 1 else None
         out = vp(8192)   # must not alias x
         r = lib.h3fp4_linear(dummy, None, None, 16, 512, 64, dummy, dummy, dummy, shift, shift, None, None, 1,
