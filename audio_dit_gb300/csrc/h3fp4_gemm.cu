@@ -146,7 +146,13 @@ struct Plan {
     static constexpr uint32_t kBarBytes = 8 * (3 * kStages + 3 + kEpiWarps + 3) + 8 + 16;
     static constexpr uint32_t kRcpOff = kBarOff + 512;          // kNvfp4: 128 fp32 block reciprocals of h;
                                                                 // kPack: of the packed activation
-    static constexpr uint32_t kSmemBytes = kRcpOff + 512;
+    // kWide: per epilogue warp the gate of its 128 columns for two segments
+    // (fp32, 1 KB) and their bias (bf16, 256 B), staged before the accumulator
+    // wait so that the epilogue -- the wide plan's critical path -- reads them
+    // from shared memory instead of waiting on global loads
+    static constexpr uint32_t kGateOff = kRcpOff + 512;
+    static constexpr uint32_t kBiasOff = kGateOff + (kWide ? kEpiWarps * 1024 : 0);
+    static constexpr uint32_t kSmemBytes = kBiasOff + (kWide ? kEpiWarps * 256 : 0);
     static_assert(kBarBytes <= 512, "barrier block");
     static_assert(kSfTmem + kStages * kSfTmemPerStage <= kTmemCols, "TMEM budget");
     static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -744,6 +750,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_2d(stg + c * kChunkBytes, &tmR, &rbar[e], nc0 + 32 * c, m0);
             }
             r_pending = p.has_resid != 0;
+            // kWide: the gate of this warp's 128 columns for the segments of its
+            // first and last rows, staged in shared memory before the accumulator
+            // wait (lanes in a third segment read it from global memory)
+            int seg_a = 0, seg_b = 0;
+            float* gst = reinterpret_cast<float*>(smem + P::kGateOff + 1024u * (uint32_t)e);
+            if (kWide && p.gate != nullptr) {
+                seg_a = segment_of_row(p.seg, min(m0, p.M - 1));
+                seg_b = segment_of_row(p.seg, min(m0 + 31, p.M - 1));
+                const int col = nc0 + 4 * lane;
+                float4 ga = make_float4(1.0f, 1.0f, 1.0f, 1.0f), gb = ga;
+                if (col < p.N) {
+                    ga = __ldg(reinterpret_cast<const float4*>(p.gate + (size_t)seg_a * p.N + col));
+                    gb = __ldg(reinterpret_cast<const float4*>(p.gate + (size_t)seg_b * p.N + col));
+                }
+                reinterpret_cast<float4*>(gst)[lane] = ga;
+                reinterpret_cast<float4*>(gst + 128)[lane] = gb;
+                __syncwarp();
+            }
+            uint8_t* bst = smem + P::kBiasOff + 256u * (uint32_t)e;  // kWide: the bias of the warp's 128 columns
+            if (kWide && p.bias != nullptr) {
+                const int col = nc0 + 4 * lane;
+                uint2 bv = make_uint2(0u, 0u);
+                if (col < p.N) bv = __ldg(reinterpret_cast<const uint2*>(p.bias + col));
+                reinterpret_cast<uint2*>(bst)[lane] = bv;
+                __syncwarp();
+            }
             bool ok = mbar_wait(acc_full, acc_phase, p.wait_ns, p.status, kStatusTimeoutEpilogue);
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) set_abort();
@@ -768,7 +800,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             const int row = m0 + lane;
             const float* grow = nullptr;
-            if (p.gate != nullptr && row < p.M) grow = p.gate + (size_t)segment_of_row(p.seg, row) * p.N;
+            const float* gsm = nullptr;  // kWide: this lane's staged gate row
+            if (p.gate != nullptr && row < p.M) {
+                const int sg = segment_of_row(p.seg, row);
+                grow = p.gate + (size_t)sg * p.N;
+                if (kWide) gsm = sg == seg_a ? gst : (sg == seg_b ? gst + 128 : nullptr);
+            }
             bool failed = false;
             uint32_t hcode[8];       // kNvfp4: this row's 64 values of h as 32 bytes of codes
             uint32_t hscale = 0u;    // kNvfp4: its four block-scale codes
@@ -888,7 +925,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint64_t y2[4];
                         {
                             uint32_t bw[4] = {0u, 0u, 0u, 0u};
-                            if (n8 < p.N && p.bias != nullptr) {
+                            if (kWide && p.bias != nullptr) {
+                                const uint4 bv = reinterpret_cast<const uint4*>(bst)[4 * c + j];
+                                bw[0] = bv.x; bw[1] = bv.y; bw[2] = bv.z; bw[3] = bv.w;
+                            } else if (n8 < p.N && p.bias != nullptr) {
                                 const uint4 bv = __ldg(reinterpret_cast<const uint4*>(p.bias + n8));
                                 bw[0] = bv.x; bw[1] = bv.y; bw[2] = bv.z; bw[3] = bv.w;
                             }
@@ -903,7 +943,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint4 rv = *slot;
                             const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
                             float4 g0 = make_float4(1.0f, 1.0f, 1.0f, 1.0f), g1 = g0;
-                            if (grow != nullptr && n8 < p.N) {
+                            if (kWide && gsm != nullptr) {
+                                g0 = reinterpret_cast<const float4*>(gsm + 32 * c + 8 * j)[0];
+                                g1 = reinterpret_cast<const float4*>(gsm + 32 * c + 8 * j)[1];
+                            } else if (grow != nullptr && n8 < p.N) {
                                 g0 = __ldg(reinterpret_cast<const float4*>(grow + n8));
                                 g1 = __ldg(reinterpret_cast<const float4*>(grow + n8) + 1);
                             }
