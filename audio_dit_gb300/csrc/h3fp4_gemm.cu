@@ -58,9 +58,10 @@
 //               shares issue slots with the producer, MMA and scale warps) and
 //               bf16 stores in two passes of two 32x32 chunks, each through two
 //               64-byte-swizzled staging buffers and TMA stores; a pass's
-//               residual chunks are TMA-loaded into those buffers first.
-//               SwiGLU: gate and up columns of 32 rows x 64 hidden units per
-//               warp, one pass.
+//               residual chunks are TMA-loaded into those buffers first (the
+//               wide plan stages all four chunks, and the gate and bias, ahead
+//               of the accumulator).  SwiGLU: gate and up columns of 32 rows x
+//               64 hidden units per warp, one pass.
 // Each kernel launch may start while the previous kernel of the stream drains
 // (programmatic dependent launch); it reads no input before griddepcontrol.wait.
 // Registers per thread (setmaxnreg): warpgroup 0: 40, scale warps: 96,
