@@ -38,7 +38,7 @@ REFERENCE_BUDGET_S = 120.0  # CPU seconds the reference arm's timed steps aim fo
 # DRAM bytes (read + write) per launch of nvfp4_gemm_kernel from one ncu capture
 # of the current kernel per workload; None where not captured.
 NCU_GEMM_TRAFFIC = {"fc1": 81.63456e6 + 757.145856e6, "fc2": 457.412352e6 + 184.280576e6,
-                    "qkv": 30.25152e6 + 99.592704e6, "attn_out": 255.282176e6 + 159.982848e6}
+                    "qkv": 30.25152e6 + 99.592704e6, "attn_out": 255.282432e6 + 160.99968e6}
 
 
 def load_peaks():
