@@ -219,6 +219,14 @@ h3fp4_status h3fp4_linear(const void* x, const void* a_sf, const float* a_gscale
     st = make_segments(seg_off, nseg <= 0 ? 1 : nseg, M, &seg);
     if (st != H3FP4_OK) return st;
     if ((st = check_device()) != H3FP4_OK) return st;
+    if (fused) {
+        // The ready flags carry this call's number, fixed at launch: a captured
+        // launch replayed from a graph would find the flags of its own previous
+        // replay already set.
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return H3FP4_ERR_CUDA;
+        if (cap != cudaStreamCaptureStatusNone) return H3FP4_ERR_INVALID;
+    }
 
     uint8_t* wsb = static_cast<uint8_t*>(ws);
     // Zeroed ahead of the quantiser so that the quantiser -> GEMM launch pair

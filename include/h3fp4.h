@@ -199,7 +199,9 @@ H3FP4_API h3fp4_status h3fp4_quantize_act(const void* x_bf16, int64_t M, int64_t
  * reported by h3fp4_check).  With the computed scale an amax pass runs
  * first; with H3FP4_GSCALE_GIVEN the GEMM kernel is the only launch.  Codes,
  * block scales, global scale and out are the bytes of the two-pass path.
- * Not with H3FP4_A_PREQUANT or H3FP4_EPI_SWIGLU; K <= 16384. */
+ * Not with H3FP4_A_PREQUANT or H3FP4_EPI_SWIGLU; K <= 16384; not on a stream
+ * being captured into a CUDA graph (H3FP4_ERR_INVALID: the flags hold a call
+ * number fixed at launch, which a replayed launch would repeat). */
 H3FP4_API h3fp4_status h3fp4_linear(const void* x, const void* a_sf, const float* a_gscale,
                           int64_t M, int64_t N, int64_t K,
                           const void* w_codes, const void* w_sf, const float* w_gscale,

@@ -172,3 +172,26 @@ def test_pack_flag_timeout_is_reported_and_context_survives():
     d = W.make_inputs("tiny", M=256)
     _, ref, out, reg_ref, reg = _pair(d)
     _assert_same(ref, out, reg_ref, reg, "after the pack timeout")
+
+
+def test_fused_refuses_stream_capture():
+    """The flags carry a call number fixed at launch, so a fused call may not be
+    captured into a graph: it is refused on the host, and the capture ends
+    cleanly (nothing was launched into it)."""
+    import audio_dit_gb300 as A
+    d = W.make_inputs("tiny", M=256)
+    case = LinearCase(d)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g.capture_begin()
+        try:
+            with pytest.raises(A.H3FP4Error) as e:
+                A.h3fp4_linear(case.x, *case.wq, case.out, case.ws, bias=case.bias, fused=True)
+            assert e.value.status == 1
+        finally:
+            g.capture_end()
+    torch.cuda.synchronize()
+    _, ref, out, reg_ref, reg = _pair(d)   # the context is intact
+    _assert_same(ref, out, reg_ref, reg, "after the refused capture")
