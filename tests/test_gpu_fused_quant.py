@@ -101,6 +101,20 @@ def test_fused_ragged_shapes(M, N, K, nseg):
     _assert_same(ref, out, reg_ref, reg, f"{M}x{N}x{K}")
 
 
+def test_fused_segments_shorter_than_a_tile():
+    """Segments of a few rows: the packer switches modulation constants inside
+    a 32-row X tile (and within a thread's rows)."""
+    d = _custom(200, 520, 256, seed=79, nseg=1)
+    seg = np.array([0, 5, 11, 20, 37, 38, 200], np.int64)
+    rng = np.random.default_rng(80)
+    d["seg_off"] = seg
+    d["shift"] = rng.standard_normal((len(seg) - 1, 256), dtype=np.float32) * 0.1
+    d["scale"] = rng.standard_normal((len(seg) - 1, 256), dtype=np.float32) * 0.1
+    d["gate"] = rng.uniform(0, 1, (len(seg) - 1, 520)).astype(np.float32)
+    _, ref, out, reg_ref, reg = _pair(d)
+    _assert_same(ref, out, reg_ref, reg, "short segments")
+
+
 @pytest.mark.parametrize("name,M", [("fc1", 520), ("attn_out", 600)])
 def test_fused_given_scale(name, M):
     """With the caller's global scale the GEMM kernel is the only launch."""

@@ -85,6 +85,23 @@ def test_ragged_shapes(orc, M, N, K):
     _full_compare(orc, _custom(M, N, K, seed=M + N + K, nseg=3 if M > 3 else 1))
 
 
+def test_segments_shorter_than_a_warp_block(orc):
+    """Segments of a few rows, so that one epilogue warp's 32 rows span three
+    or more segments: with the gated epilogue over a short K loop the kernel
+    stages the gate of the block's first and last segments in shared memory
+    and reads the others from global memory."""
+    d = _custom(200, 520, 256, seed=77, nseg=1)
+    seg = np.array([0, 5, 11, 20, 37, 38, 200], np.int64)
+    nseg = len(seg) - 1
+    rng = np.random.default_rng(78)
+    d["seg_off"] = seg
+    d["workload"] = W.Workload("custom_short_segments", 200, 256, 520, 77, True, True, True, "short segments")
+    d["shift"] = rng.standard_normal((nseg, 256), dtype=np.float32) * 0.1
+    d["scale"] = rng.standard_normal((nseg, 256), dtype=np.float32) * 0.1
+    d["gate"] = rng.uniform(0, 1, (nseg, 520)).astype(np.float32)
+    _full_compare(orc, d)
+
+
 def test_no_bias_no_prologue(orc):
     d = _custom(200, 512, 512, seed=5, gated=False, mod=False)
     case = LinearCase(d, use_bias=False)
