@@ -101,11 +101,13 @@ def test_fused_ragged_shapes(M, N, K, nseg):
     _assert_same(ref, out, reg_ref, reg, f"{M}x{N}x{K}")
 
 
-def test_fused_segments_shorter_than_a_tile():
-    """Segments of a few rows: the packer switches modulation constants inside
-    a 32-row X tile (and within a thread's rows)."""
+@pytest.mark.parametrize("seg", [[0, 5, 11, 20, 37, 38, 200], [0, 3, 3, 4, 40, 41, 100, 163, 200]])
+def test_fused_segments_shorter_than_a_tile(seg):
+    """Segments of a few rows (up to the most the boundary accepts, one empty):
+    the packer switches modulation constants inside a 32-row X tile (and
+    within a thread's rows)."""
     d = _custom(200, 520, 256, seed=79, nseg=1)
-    seg = np.array([0, 5, 11, 20, 37, 38, 200], np.int64)
+    seg = np.array(seg, np.int64)
     rng = np.random.default_rng(80)
     d["seg_off"] = seg
     d["shift"] = rng.standard_normal((len(seg) - 1, 256), dtype=np.float32) * 0.1

@@ -85,13 +85,18 @@ def test_ragged_shapes(orc, M, N, K):
     _full_compare(orc, _custom(M, N, K, seed=M + N + K, nseg=3 if M > 3 else 1))
 
 
-def test_segments_shorter_than_a_warp_block(orc):
+SHORT_SEGMENTS = [[0, 5, 11, 20, 37, 38, 200],
+                  [0, 3, 3, 4, 40, 41, 100, 163, 200]]  # the most segments, one empty, one a single row
+
+
+@pytest.mark.parametrize("seg", SHORT_SEGMENTS)
+def test_segments_shorter_than_a_warp_block(orc, seg):
     """Segments of a few rows, so that one epilogue warp's 32 rows span three
     or more segments: with the gated epilogue over a short K loop the kernel
     stages the gate of the block's first and last segments in shared memory
     and reads the others from global memory."""
     d = _custom(200, 520, 256, seed=77, nseg=1)
-    seg = np.array([0, 5, 11, 20, 37, 38, 200], np.int64)
+    seg = np.array(seg, np.int64)
     nseg = len(seg) - 1
     rng = np.random.default_rng(78)
     d["seg_off"] = seg

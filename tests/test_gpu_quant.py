@@ -53,6 +53,25 @@ def test_gscale_given(orc):
         assert_quant_equal(gpu, ref, f"given {gs}")
 
 
+def test_max_segments_with_empty_and_single_row_segments(orc):
+    """The largest segment table the boundary accepts, with an empty segment
+    and a one-row segment: every row takes its own segment's vectors, and the
+    empty segment's vectors are never used."""
+    import audio_dit_gb300 as A
+    M, K = 200, 1024
+    seg = np.array([0, 3, 3, 4, 40, 41, 100, 163, 200], np.int64)
+    nseg = len(seg) - 1
+    assert nseg == A.MAX_SEGMENTS
+    rng = np.random.default_rng(201)
+    x = W.to_bf16_bits(rng.standard_normal((M, K), dtype=np.float32))
+    shift = rng.standard_normal((nseg, K), dtype=np.float32) * 0.1
+    scale = rng.standard_normal((nseg, K), dtype=np.float32) * 0.1
+    shift[1] = 1e6  # the empty segment: using it for any row would show
+    ref = orc.quantize(x, shift, scale, seg)
+    gpu = gpu_quantize(x, shift, scale, seg)
+    assert_quant_equal(gpu, ref, f"{nseg} segments")
+
+
 @pytest.mark.parametrize("M,K", [(1, 64), (7, 128), (127, 3072), (128, 64), (129, 512), (946, 3072), (5, 12288)])
 def test_edge_rows(orc, M, K):
     rng = np.random.default_rng(M * 7 + K)
